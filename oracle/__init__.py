@@ -1,0 +1,134 @@
+"""fp64 CPU oracle for scaled-dot-product attention forward.
+
+TEST INFRASTRUCTURE.  Only the test suite, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The library under
+``flash_attention_forward_gb300`` never imports it and shares no code with it.
+
+The arithmetic lives in ``oracle.cpp`` (plain two-pass fp64 softmax, one query
+row at a time).  This wrapper only converts tensors to fp64 exactly as the GPU
+sees them (fp16/bf16 values as stored; e4m3 codes times their per-tensor scale,
+through torch's own float8 cast) and calls the C entry points.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.cpp")
+_OUT = os.path.join(_HERE, "_obj", "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.cpp into oracle/_obj/liboracle.so (plain g++, no fast-math)."""
+    os.makedirs(os.path.dirname(_OUT), exist_ok=True)
+    if not force and os.path.exists(_OUT) and os.path.getmtime(_OUT) >= os.path.getmtime(_SRC):
+        return _OUT
+    tmp = _OUT + f".{os.getpid()}.tmp"
+    cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread", "-fno-fast-math", _SRC, "-o", tmp]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _OUT)
+    return _OUT
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            d, i64, p = ctypes.c_double, ctypes.c_int64, ctypes.c_void_p
+            lib.oracle_sdpa_fwd.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, i64, i64, i64, d, ctypes.c_int,
+                                            p, i64, ctypes.c_int]
+            lib.oracle_sdpa_fwd.restype = ctypes.c_int
+            lib.oracle_sdpa_decode.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, i64, i64, d, ctypes.c_int]
+            lib.oracle_sdpa_decode.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def as_f64(t, scale: float = 1.0) -> np.ndarray:
+    """Exact fp64 view of stored values (times a per-tensor scale for e4m3 codes)."""
+    if isinstance(t, np.ndarray):
+        a = t.astype(np.float64, copy=False)
+    else:
+        a = t.detach().to("cpu").to(torch.float64).numpy()
+    if scale != 1.0:
+        a = a * float(scale)
+    return np.ascontiguousarray(a)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def sdpa_fwd(q, k, v, mask=None, *, scale: float, causal: bool = False, rows=None, descale=(1.0, 1.0, 1.0),
+             nthreads: int | None = None):
+    """O and LSE of softmax(scale * Q K^T + mask) V in fp64.
+
+    q [B,Sq,Hq,D], k [B,Sk,Hkv,D], v [B,Sk,Hkv,Dv], mask [B,Sq,Sk] or None.
+    rows: optional int array [n, 3] of (b, h, i); then O is [n, Dv] and LSE [n].
+    Otherwise O is [B,Sq,Hq,Dv] and LSE [B,Hq,Sq]."""
+    qd, kd, vd = as_f64(q, descale[0]), as_f64(k, descale[1]), as_f64(v, descale[2])
+    md = None if mask is None else as_f64(mask)
+    B, Sq, Hq, D = qd.shape
+    _, Sk, Hkv, _ = kd.shape
+    Dv = vd.shape[-1]
+    if md is not None:
+        assert md.shape == (B, Sq, Sk), md.shape
+    if rows is not None:
+        r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+        n = r.shape[0]
+        o = np.empty((n, Dv), dtype=np.float64)
+        lse = np.empty((n,), dtype=np.float64)
+    else:
+        r, n = None, 0
+        o = np.empty((B, Sq, Hq, Dv), dtype=np.float64)
+        lse = np.empty((B, Hq, Sq), dtype=np.float64)
+    rc = _load().oracle_sdpa_fwd(_ptr(qd), _ptr(kd), _ptr(vd), _ptr(md), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Sk, D,
+                                 Dv, float(scale), int(bool(causal)), _ptr(r), n, nthreads or threads())
+    if rc != 0:
+        raise ValueError("oracle_sdpa_fwd: invalid arguments")
+    return o, lse
+
+
+def sdpa_decode(q, k_cache, v_cache, kv_len, *, scale: float, batches=None, nthreads: int | None = None):
+    """Decode oracle: q [B,Hq,D], caches [B,max_kv,Hkv,.], kv_len [B].
+
+    Only the first kv_len[b] cache rows of each sequence are converted and read.  ``batches``
+    restricts the work to a subset of sequences; the result then has len(batches) rows."""
+    kvl = [int(x) for x in (kv_len.tolist() if hasattr(kv_len, "tolist") else kv_len)]
+    B, Hq, D = q.shape
+    Hkv = k_cache.shape[2]
+    Dv = v_cache.shape[-1]
+    sel = list(range(B)) if batches is None else [int(b) for b in batches]
+    o = np.empty((len(sel), Hq, Dv), dtype=np.float64)
+    lse = np.empty((len(sel), Hq), dtype=np.float64)
+    lib = _load()
+    for n, b in enumerate(sel):
+        L = kvl[b]
+        qd = as_f64(q[b:b + 1])
+        kd = as_f64(k_cache[b:b + 1, :L])
+        vd = as_f64(v_cache[b:b + 1, :L])
+        kl = np.array([L], dtype=np.int32)
+        ob = np.empty((1, Hq, Dv), dtype=np.float64)
+        lb = np.empty((1, Hq), dtype=np.float64)
+        rc = lib.oracle_sdpa_decode(_ptr(qd), _ptr(kd), _ptr(vd), _ptr(kl), _ptr(ob), _ptr(lb), 1, Hq, Hkv, L, D, Dv,
+                                    float(scale), nthreads or threads())
+        if rc != 0:
+            raise ValueError("oracle_sdpa_decode: invalid arguments")
+        o[n], lse[n] = ob[0], lb[0]
+    return o, lse

@@ -1,0 +1,272 @@
+"""Pins for the fp64 oracle, independent of the oracle itself.
+
+Each test checks the oracle against something the mathematics fixes: closed
+forms, invariants, exhaustive tiny grids against torch's own fp64
+scaled_dot_product_attention, and hand-derived values.  A plausible slip in the
+oracle (a dropped mask or max term, a wrong GQA index, a causal off-by-one, a
+transposed operand, a missing 1/l) fails at least one of them.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+import workloads
+
+NEG_INF = float("-inf")
+
+
+def _rand(shape, seed, lo=-1.0, hi=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.rand(shape, generator=g, dtype=torch.float64) * (hi - lo) + lo)
+
+
+def _torch_sdpa(q, k, v, mask, scale, causal):
+    """torch's fp64 reference on [B,S,H,D] tensors (GQA through enable_gqa)."""
+    qt, kt, vt = (x.transpose(1, 2) for x in (q, k, v))
+    am = None if mask is None else mask.unsqueeze(1)
+    if am is not None and causal:
+        Sq, Sk = q.shape[1], k.shape[1]
+        keep = torch.ones(Sq, Sk, dtype=torch.bool).tril()
+        am, causal = am.masked_fill(~keep, NEG_INF), False
+    o = F.scaled_dot_product_attention(qt, kt, vt, attn_mask=am, is_causal=causal, scale=scale,
+                                       enable_gqa=q.shape[2] != k.shape[2])
+    return o.transpose(1, 2)
+
+
+def _torch_lse(q, k, mask, scale, causal):
+    group = q.shape[2] // k.shape[2]
+    kr = k.repeat_interleave(group, dim=2)
+    s = torch.einsum("bihd,bjhd->bhij", q, kr) * scale
+    if mask is not None:
+        s = s + mask.unsqueeze(1)
+    if causal:
+        Sq, Sk = s.shape[-2:]
+        keep = torch.ones(Sq, Sk, dtype=torch.bool).tril()
+        s = s.masked_fill(~keep, NEG_INF)
+    return torch.logsumexp(s, dim=-1)
+
+
+def test_hand_worked_two_keys():
+    # q = (1, 0), k0 = (2, 0), k1 = (0, 3), scale = 1/2  ->  s = (1, 0)
+    q = torch.tensor([1.0, 0.0], dtype=torch.float64).view(1, 1, 1, 2)
+    k = torch.tensor([[2.0, 0.0], [0.0, 3.0]], dtype=torch.float64).view(1, 2, 1, 2)
+    v = torch.tensor([[1.0, -1.0], [3.0, 5.0]], dtype=torch.float64).view(1, 2, 1, 2)
+    o, lse = oracle.sdpa_fwd(q, k, v, scale=0.5)
+    e = math.e
+    want = [(e * 1.0 + 3.0) / (e + 1.0), (e * -1.0 + 5.0) / (e + 1.0)]
+    assert np.allclose(o.reshape(-1), want, rtol=0, atol=1e-15)
+    assert abs(lse.item() - math.log(e + 1.0)) < 1e-15
+    # causal: query 0 sees key 0 only
+    o, lse = oracle.sdpa_fwd(q, k, v, scale=0.5, causal=True)
+    assert np.allclose(o.reshape(-1), [1.0, -1.0], atol=0)
+    assert lse.item() == pytest.approx(1.0, abs=1e-15)
+
+
+def test_huge_scores_do_not_overflow():
+    # scores 1000 and 999: a missing max subtraction overflows exp to inf -> nan
+    q = torch.tensor([1.0], dtype=torch.float64).view(1, 1, 1, 1)
+    k = torch.tensor([[1000.0], [999.0]], dtype=torch.float64).view(1, 2, 1, 1)
+    v = torch.tensor([[0.0], [1.0]], dtype=torch.float64).view(1, 2, 1, 1)
+    o, lse = oracle.sdpa_fwd(q, k, v, scale=1.0)
+    w1 = math.exp(-1.0) / (1.0 + math.exp(-1.0))
+    assert o.item() == pytest.approx(w1, abs=1e-15)
+    assert lse.item() == pytest.approx(1000.0 + math.log1p(math.exp(-1.0)), abs=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_single_key_returns_v_row(causal):
+    B, Sq, Hq, Hkv, D, Dv = 2, 5, 4, 2, 7, 3
+    q, k, v = _rand((B, Sq, Hq, D), 1), _rand((B, 1, Hkv, D), 2), _rand((B, 1, Hkv, Dv), 3)
+    mask = _rand((B, Sq, 1), 4)
+    o, lse = oracle.sdpa_fwd(q, k, v, mask, scale=0.3, causal=causal)
+    for b in range(B):
+        for h in range(Hq):
+            kvh = h // (Hq // Hkv)
+            for i in range(Sq):
+                assert np.array_equal(o[b, i, h], v[b, 0, kvh].numpy())
+                want = 0.3 * float(q[b, i, h] @ k[b, 0, kvh]) + float(mask[b, i, 0])
+                assert lse[b, h, i] == pytest.approx(want, abs=1e-14)
+
+
+def test_constant_v_rows_give_that_row():
+    B, Sq, Sk, Hq, Hkv, D, Dv = 1, 9, 13, 2, 1, 5, 6
+    q, k = _rand((B, Sq, Hq, D), 5, -3, 3), _rand((B, Sk, Hkv, D), 6, -3, 3)
+    row = _rand((Dv,), 7)
+    v = row.view(1, 1, 1, Dv).expand(B, Sk, Hkv, Dv).contiguous()
+    for causal in (False, True):
+        o, _ = oracle.sdpa_fwd(q, k, v, scale=0.7, causal=causal)
+        assert np.allclose(o, row.numpy().reshape(1, 1, 1, Dv), atol=1e-14, rtol=0)
+
+
+@pytest.mark.parametrize("Sq,Sk", [(6, 6), (4, 9), (9, 4)])
+def test_zero_query_is_mean_of_visible_rows(Sq, Sk):
+    B, Hq, Hkv, D, Dv = 2, 3, 3, 4, 5
+    q = torch.zeros((B, Sq, Hq, D), dtype=torch.float64)
+    k, v = _rand((B, Sk, Hkv, D), 8), _rand((B, Sk, Hkv, Dv), 9)
+    o, lse = oracle.sdpa_fwd(q, k, v, scale=1.0, causal=False)
+    assert np.allclose(o, v.mean(dim=1, keepdim=True).numpy(), atol=1e-14)
+    assert np.allclose(lse, math.log(Sk), atol=1e-14)
+    o, lse = oracle.sdpa_fwd(q, k, v, scale=1.0, causal=True)
+    for i in range(Sq):
+        n = min(i + 1, Sk)  # top-left causal: key j visible iff j <= i
+        assert np.allclose(o[:, i], v[:, :n].mean(dim=1).numpy(), atol=1e-14)
+        assert np.allclose(lse[:, :, i], math.log(n), atol=1e-14)
+
+
+def test_causal_first_row_is_first_v_row():
+    B, Sq, Sk, Hq, Hkv, D, Dv = 2, 7, 7, 4, 2, 8, 8
+    q, k, v = _rand((B, Sq, Hq, D), 10, -4, 4), _rand((B, Sk, Hkv, D), 11, -4, 4), _rand((B, Sk, Hkv, Dv), 12)
+    o, _ = oracle.sdpa_fwd(q, k, v, scale=1.0, causal=True)
+    for h in range(Hq):
+        assert np.array_equal(o[:, 0, h], v[:, 0, h // 2].numpy())
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_identity_v_exposes_probabilities(causal):
+    # V = I (Dv = Sk) turns O into the probability matrix itself
+    B, Sq, Sk, H, D = 1, 6, 8, 1, 4
+    q, k = _rand((B, Sq, H, D), 13, -2, 2), _rand((B, Sk, H, D), 14, -2, 2)
+    mask = _rand((B, Sq, Sk), 15)
+    v = torch.eye(Sk, dtype=torch.float64).view(1, Sk, 1, Sk)
+    o, _ = oracle.sdpa_fwd(q, k, v, mask, scale=0.9, causal=causal)
+    P = o[0, :, 0, :]
+    assert np.allclose(P.sum(axis=1), 1.0, atol=1e-14)
+    s = 0.9 * (q[0, :, 0] @ k[0, :, 0].T) + mask[0]
+    if causal:
+        s = s.masked_fill(~torch.ones(Sq, Sk, dtype=torch.bool).tril(), NEG_INF)
+        assert np.all(P[np.triu_indices(Sq, 1, Sk)] == 0.0)
+    assert np.allclose(P, torch.softmax(s, dim=-1).numpy(), atol=1e-15)
+
+
+def test_joint_permutation_of_keys_is_invariant():
+    B, Sq, Sk, Hq, Hkv, D, Dv = 2, 5, 11, 4, 2, 6, 7
+    q, k, v = _rand((B, Sq, Hq, D), 16), _rand((B, Sk, Hkv, D), 17), _rand((B, Sk, Hkv, Dv), 18)
+    mask = _rand((B, Sq, Sk), 19)
+    perm = torch.randperm(Sk, generator=torch.Generator().manual_seed(20))
+    o1, l1 = oracle.sdpa_fwd(q, k, v, mask, scale=0.4)
+    o2, l2 = oracle.sdpa_fwd(q, k[:, perm], v[:, perm], mask[:, :, perm], scale=0.4)
+    assert np.allclose(o1, o2, atol=1e-14) and np.allclose(l1, l2, atol=1e-14)
+    # a permutation of K alone (V not moved) must change the result
+    o3, _ = oracle.sdpa_fwd(q, k[:, perm], v, mask, scale=0.4)
+    assert not np.allclose(o1, o3, atol=1e-6)
+
+
+def test_mask_shift_moves_lse_only():
+    B, Sq, Sk, Hq, D, Dv = 1, 4, 9, 2, 5, 3
+    q, k, v = _rand((B, Sq, Hq, D), 21), _rand((B, Sk, Hq, D), 22), _rand((B, Sk, Hq, Dv), 23)
+    mask = _rand((B, Sq, Sk), 24)
+    o1, l1 = oracle.sdpa_fwd(q, k, v, mask, scale=1.1, causal=True)
+    o2, l2 = oracle.sdpa_fwd(q, k, v, mask + 2.5, scale=1.1, causal=True)
+    assert np.allclose(o1, o2, atol=1e-14)
+    assert np.allclose(l2, l1 + 2.5, atol=1e-13)
+
+
+def test_fully_masked_rows_are_zero_without_nan():
+    B, Sq, Sk, Hq, Hkv, D, Dv = 2, 6, 10, 4, 2, 8, 8
+    q, k, v = _rand((B, Sq, Hq, D), 25), _rand((B, Sk, Hkv, D), 26), _rand((B, Sk, Hkv, Dv), 27)
+    mask = torch.zeros((B, Sq, Sk), dtype=torch.float64)
+    mask[0, 2, :] = NEG_INF
+    mask[1, 5, :] = NEG_INF
+    mask[1, 0, 3:] = NEG_INF  # partially masked row stays finite
+    o, lse = oracle.sdpa_fwd(q, k, v, mask, scale=0.5)
+    assert not np.isnan(o).any() and not np.isnan(lse).any()
+    assert np.all(o[0, 2] == 0.0) and np.all(o[1, 5] == 0.0)
+    assert np.all(lse[0, :, 2] == NEG_INF) and np.all(lse[1, :, 5] == NEG_INF)
+    assert np.isfinite(lse[1, :, 0]).all()
+    # with causal on top, row 0 of batch 1 sees key 0 only -> but key 0 is visible there
+    mask2 = mask.clone()
+    mask2[1, 0, 0] = NEG_INF
+    o, lse = oracle.sdpa_fwd(q, k, v, mask2, scale=0.5, causal=True)
+    assert np.all(o[1, 0] == 0.0) and np.all(lse[1, :, 0] == NEG_INF)
+
+
+def test_gqa_equals_mha_with_repeated_heads():
+    B, Sq, Sk, Hq, Hkv, D, Dv = 2, 7, 9, 6, 2, 5, 4
+    q, k, v = _rand((B, Sq, Hq, D), 28), _rand((B, Sk, Hkv, D), 29), _rand((B, Sk, Hkv, Dv), 30)
+    o1, l1 = oracle.sdpa_fwd(q, k, v, scale=0.8, causal=True)
+    g = Hq // Hkv
+    o2, l2 = oracle.sdpa_fwd(q, k.repeat_interleave(g, dim=2), v.repeat_interleave(g, dim=2), scale=0.8,
+                             causal=True)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    # interleaved mapping (h % Hkv) would differ
+    o3, _ = oracle.sdpa_fwd(q, k.repeat(1, 1, g, 1), v.repeat(1, 1, g, 1), scale=0.8, causal=True)
+    assert not np.allclose(o1, o3, atol=1e-6)
+
+
+@pytest.mark.parametrize("Sk", [1, 2, 127, 128, 129])
+@pytest.mark.parametrize("Sq", [1, 15, 16, 17])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("use_mask", [False, True])
+def test_matches_torch_sdpa_fp64(Sq, Sk, causal, use_mask):
+    # the page "Xe2 ESIMD Flash Attention", section "Workflow", lists these corner cases:
+    # q not 16-aligned, kv not chunk-aligned, kv not 8-aligned, kv shorter than a chunk
+    B, Hq, Hkv, D, Dv = 2, 4, 2, 8, 6
+    seed = 1000 * Sq + Sk + 7 * causal + 3 * use_mask
+    q, k, v = _rand((B, Sq, Hq, D), seed, -2, 2), _rand((B, Sk, Hkv, D), seed + 1, -2, 2), \
+        _rand((B, Sk, Hkv, Dv), seed + 2)
+    mask = None
+    if use_mask:
+        g = torch.Generator().manual_seed(seed + 3)
+        mask = torch.where(torch.rand((B, Sq, Sk), generator=g) < 0.2, NEG_INF, 0.0).to(torch.float64)
+        mask[:, :, 0] = _rand((B, Sq), seed + 4)  # key 0 never -inf: no fully masked rows here
+    scale = 1.0 / math.sqrt(D)
+    o, lse = oracle.sdpa_fwd(q, k, v, mask, scale=scale, causal=causal)
+    ref = _torch_sdpa(q, k, v, mask, scale, causal).numpy()
+    assert np.abs(o - ref).max() <= 1e-12
+    ref_lse = _torch_lse(q, k, mask, scale, causal).numpy()
+    assert np.abs(lse - ref_lse).max() <= 1e-12
+
+
+def test_row_subset_matches_full():
+    B, Sq, Sk, Hq, Hkv, D, Dv = 2, 33, 40, 4, 1, 16, 8
+    q, k, v = _rand((B, Sq, Hq, D), 31), _rand((B, Sk, Hkv, D), 32), _rand((B, Sk, Hkv, Dv), 33)
+    o, lse = oracle.sdpa_fwd(q, k, v, scale=0.25, causal=True)
+    rows = np.array([[0, 0, 0], [1, 3, 32], [0, 2, 17], [1, 1, 5]])
+    os_, ls = oracle.sdpa_fwd(q, k, v, scale=0.25, causal=True, rows=rows)
+    for n, (b, h, i) in enumerate(rows):
+        assert np.array_equal(os_[n], o[b, i, h]) and ls[n] == lse[b, h, i]
+
+
+def test_decode_matches_torch_per_sequence():
+    B, Hq, Hkv, max_kv, D, Dv = 3, 8, 2, 50, 16, 16
+    kv_len = torch.tensor([50, 1, 23], dtype=torch.int32)
+    q = _rand((B, Hq, D), 34)
+    k, v = _rand((B, max_kv, Hkv, D), 35), _rand((B, max_kv, Hkv, Dv), 36)
+    k[1, 1:] = float("nan")  # padding must never be read
+    v[2, 23:] = float("nan")
+    o, lse = oracle.sdpa_decode(q, k, v, kv_len, scale=0.25)
+    for b in range(B):
+        L = int(kv_len[b])
+        ref = _torch_sdpa(q[b:b + 1, None], k[b:b + 1, :L], v[b:b + 1, :L], None, 0.25, False)
+        assert np.abs(o[b] - ref[0, 0].numpy()).max() <= 1e-12
+        ref_lse = _torch_lse(q[b:b + 1, None], k[b:b + 1, :L], None, 0.25, False)
+        assert np.abs(lse[b] - ref_lse[0, :, 0].numpy()).max() <= 1e-12
+    o2, _ = oracle.sdpa_decode(q, k, v, kv_len, scale=0.25, batches=[2, 0])
+    assert np.array_equal(o2[0], o[2]) and np.array_equal(o2[1], o[0])
+
+
+def test_e4m3_inputs_are_codes_times_scale():
+    # the oracle reads e4m3 codes through torch's float8 cast, times the per-tensor scale
+    x = torch.tensor([0.0, 1.0, -2.5, 448.0, 0.001953125, -0.875], dtype=torch.float32)
+    codes = x.to(torch.float8_e4m3fn)
+    got = oracle.as_f64(codes, 0.5)
+    assert np.array_equal(got, np.array([0.0, 0.5, -1.25, 224.0, 0.0009765625, -0.4375]))
+
+
+def test_workload_inputs_are_seeded_and_exact():
+    w = workloads.WORKLOADS["tiny_prefill_f16_d64"]
+    a, b = workloads.prefill_inputs(w), workloads.prefill_inputs(w)
+    assert all(torch.equal(a[n], b[n]) for n in ("q", "k", "v"))
+    assert a["q"].dtype == torch.float16 and a["q"].shape == (1, 512, 1, 64)
+    assert float(a["q"].abs().max()) <= 1.0
+    c = workloads.prefill_inputs(w, rotation=1)
+    assert not torch.equal(a["q"], c["q"])
+    m = workloads.make_mask(workloads.generator(3), 2, 100, 300, 0.1, 0.05)
+    full = torch.isinf(m).all(dim=-1)
+    assert int(full[0].sum()) >= 5 and int(full[1].sum()) >= 5
+    frac = float(torch.isinf(m[~full]).float().mean())
+    assert 0.08 < frac < 0.12

@@ -1,0 +1,173 @@
+"""Seeded synthetic inputs for the attention workloads.
+
+This module only draws random numbers and lays them out; it holds none of the
+attention arithmetic.  The CUDA path (through the Python binding) and the fp64
+oracle both consume the tensors made here, so both sides see bit-identical
+inputs.
+
+Seeds: every buffer set of workload ``index`` c and rotation r is drawn from
+``torch.Generator('cpu').manual_seed(1000 * c + r)``.  Draw order is q, k, v,
+then the mask (prefill); for decode it is q, kv_len, then per sequence the
+valid K rows followed by the valid V rows (padding rows are never drawn).
+Uniform[-1, 1] is ``2 * rand - 1`` in fp32; N(0, 1) is ``randn`` in fp32; the
+cast to the stored type rounds to nearest even.  FP8 e4m3 codes are the
+saturating RNE cast of ``x / s`` with the per-tensor scale ``s = amax / 448``.
+
+The workload shapes follow the page "Xe2 ESIMD Flash Attention - SDP Prefill &
+Decode", sections "GQA layout" (Q [q_len, headQ, HD], K/V [kv_len, headKv, HD])
+and "Workflow" (small correctness size q=512, kv=1024), extended with a batch
+dimension.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field, replace
+
+import torch
+
+E4M3_MAX = 448.0
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    index: int            # 1-based workload number, feeds the seed
+    kind: str             # "prefill" | "decode"
+    B: int
+    Hq: int
+    Hkv: int
+    Sq: int               # decode: 1
+    Sk: int               # decode: padded cache length (max_kv)
+    D: int
+    Dv: int
+    dtype: str            # "f16" | "bf16" | "e4m3"
+    dist: str             # "uniform" | "normal"
+    causal: bool = False
+    mask: bool = False
+    out_dtype: str = "bf16"
+    kv_len_range: tuple = ()      # decode only: inclusive [lo, hi]
+    masked_frac: float = 0.0      # additive mask: fraction of -inf entries
+    full_row_frac: float = 0.0    # additive mask: fraction of fully -inf query rows
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    def with_shape(self, **kw) -> "Workload":
+        return replace(self, **kw)
+
+
+WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("tiny_prefill_f16_d64", 1, "prefill", B=1, Hq=1, Hkv=1, Sq=512, Sk=1024, D=64, Dv=64,
+                 dtype="f16", dist="uniform", out_dtype="f16"),
+        Workload("gqa_causal_prefill_bf16_d128", 2, "prefill", B=2, Hq=32, Hkv=8, Sq=4096, Sk=4096, D=128,
+                 Dv=128, dtype="bf16", dist="normal", causal=True, out_dtype="bf16"),
+        Workload("unaligned_mask_prefill_bf16_d128", 3, "prefill", B=3, Hq=28, Hkv=4, Sq=1000, Sk=3001, D=128,
+                 Dv=128, dtype="bf16", dist="normal", mask=True, out_dtype="bf16", masked_frac=0.10,
+                 full_row_frac=0.05),
+        Workload("splitkv_decode_bf16_d128", 4, "decode", B=64, Hq=32, Hkv=8, Sq=1, Sk=16384, D=128, Dv=128,
+                 dtype="bf16", dist="normal", out_dtype="bf16", kv_len_range=(1024, 16384)),
+        Workload("mla_fp8_causal_prefill_d192", 5, "prefill", B=1, Hq=128, Hkv=128, Sq=8192, Sk=8192, D=192,
+                 Dv=128, dtype="e4m3", dist="normal", causal=True, out_dtype="bf16"),
+    ]
+}
+
+BY_INDEX = {w.index: w for w in WORKLOADS.values()}
+
+_TORCH_DTYPE = {"f16": torch.float16, "bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn}
+
+
+def torch_dtype(name: str) -> torch.dtype:
+    return _TORCH_DTYPE[name]
+
+
+def generator(index: int, rotation: int = 0) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(1000 * index + rotation)
+    return g
+
+
+def _draw(g: torch.Generator, shape, dist: str) -> torch.Tensor:
+    if dist == "uniform":
+        return torch.rand(shape, generator=g, dtype=torch.float32) * 2.0 - 1.0
+    if dist == "normal":
+        return torch.randn(shape, generator=g, dtype=torch.float32)
+    raise ValueError(dist)
+
+
+def quantize_e4m3(x: torch.Tensor):
+    """Per-tensor e4m3 quantisation of an fp32 tensor: (codes, scale) with x ~= codes * scale."""
+    amax = float(x.abs().max())
+    s = amax / E4M3_MAX if amax > 0 else 1.0
+    codes = (x / s).to(torch.float8_e4m3fn)
+    return codes, s
+
+
+def _store(x: torch.Tensor, dtype: str):
+    if dtype == "e4m3":
+        return quantize_e4m3(x)
+    return x.to(_TORCH_DTYPE[dtype]), 1.0
+
+
+def make_mask(g: torch.Generator, B: int, Sq: int, Sk: int, masked_frac: float, full_row_frac: float):
+    """Additive fp16 mask [B, Sq, Sk] of 0 / -inf: each entry -inf with probability ``masked_frac``,
+    then round(full_row_frac * Sq) query rows per batch (a seeded permutation) set entirely -inf."""
+    m = torch.zeros((B, Sq, Sk), dtype=torch.float16)
+    hit = torch.rand((B, Sq, Sk), generator=g, dtype=torch.float32) < masked_frac
+    m[hit] = float("-inf")
+    n_full = int(round(full_row_frac * Sq))
+    for b in range(B):
+        rows = torch.randperm(Sq, generator=g)[:n_full]
+        m[b, rows, :] = float("-inf")
+    return m
+
+
+def prefill_inputs(w: Workload, rotation: int = 0):
+    """Q [B,Sq,Hq,D], K [B,Sk,Hkv,D], V [B,Sk,Hkv,Dv] (stored dtype) plus optional mask [B,Sq,Sk] fp16.
+
+    For e4m3 the per-tensor scales are returned in ``descale`` = (s_q, s_k, s_v)."""
+    assert w.kind == "prefill"
+    g = generator(w.index, rotation)
+    q, sq = _store(_draw(g, (w.B, w.Sq, w.Hq, w.D), w.dist), w.dtype)
+    k, sk = _store(_draw(g, (w.B, w.Sk, w.Hkv, w.D), w.dist), w.dtype)
+    v, sv = _store(_draw(g, (w.B, w.Sk, w.Hkv, w.Dv), w.dist), w.dtype)
+    mask = make_mask(g, w.B, w.Sq, w.Sk, w.masked_frac, w.full_row_frac) if w.mask else None
+    return {"q": q, "k": k, "v": v, "mask": mask, "descale": (sq, sk, sv)}
+
+
+def decode_inputs(w: Workload, rotation: int = 0, pad_value: float = float("nan"), kv_len=None):
+    """q [B,Hq,D], padded caches [B,max_kv,Hkv,D|Dv], kv_len int32 [B].
+
+    Rows at or beyond kv_len[b] hold ``pad_value`` (NaN by default, so a kernel that reads them
+    poisons its output)."""
+    assert w.kind == "decode"
+    g = generator(w.index, rotation)
+    dt = _TORCH_DTYPE[w.dtype]
+    q = _draw(g, (w.B, w.Hq, w.D), w.dist).to(dt)
+    if kv_len is None:
+        lo, hi = w.kv_len_range
+        kv_len = torch.randint(lo, hi + 1, (w.B,), generator=g, dtype=torch.int64).to(torch.int32)
+    else:
+        kv_len = torch.as_tensor(kv_len, dtype=torch.int32)
+    k = torch.full((w.B, w.Sk, w.Hkv, w.D), pad_value, dtype=dt)
+    v = torch.full((w.B, w.Sk, w.Hkv, w.Dv), pad_value, dtype=dt)
+    for b in range(w.B):
+        n = int(kv_len[b])
+        k[b, :n] = _draw(g, (n, w.Hkv, w.D), w.dist).to(dt)
+        v[b, :n] = _draw(g, (n, w.Hkv, w.Dv), w.dist).to(dt)
+    return {"q": q, "k": k, "v": v, "kv_len": kv_len}
+
+
+def custom_prefill(B, Hq, Hkv, Sq, Sk, D, Dv, dtype="bf16", dist="normal", seed=0, mask=False,
+                   masked_frac=0.1, full_row_frac=0.05):
+    """Small prefill cases for tests: same recipe, explicit seed."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    q, sq = _store(_draw(g, (B, Sq, Hq, D), dist), dtype)
+    k, sk = _store(_draw(g, (B, Sk, Hkv, D), dist), dtype)
+    v, sv = _store(_draw(g, (B, Sk, Hkv, Dv), dist), dtype)
+    m = make_mask(g, B, Sq, Sk, masked_frac, full_row_frac) if mask else None
+    return {"q": q, "k": k, "v": v, "mask": m, "descale": (sq, sk, sv)}
