@@ -1,0 +1,212 @@
+"""GB300 (sm_103a) fused scaled-dot-product-attention forward.
+
+Thin Python binding over the C ABI in ``include/sdpa.h`` (library
+``libsdpa_gb300.so``, built in-tree by ``flash_attention_forward_gb300.build``).
+The binding only marshals arguments: it reads shapes, strides and data pointers of
+torch tensors, allocates outputs and scratch with torch when the caller does not
+pass them, and calls the library on the current CUDA stream.  Every step of the
+computation runs in the library's kernels; there is no fallback.
+
+Entry points (same names as the C ABI):
+    sdpa_fwd(q, k, v, ...)                     fp16 / bf16 prefill
+    sdpa_fwd_fp8(q, k, v, dq, dk, dv, ...)     e4m3 prefill with per-tensor scales
+    sdpa_decode(q, k_cache, v_cache, kv_len, ...)   two-phase split-KV decode
+    sdpa_fwd_workspace_size, sdpa_decode_workspace_size, sdpa_check_device_status,
+    sdpa_status_string, sdpa_version
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsdpa_gb300.so")
+HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "sdpa.h")
+
+SDPA_OK, SDPA_ERR_INVALID, SDPA_ERR_UNSUPPORTED, SDPA_ERR_CUDA, SDPA_ERR_TIMEOUT = range(5)
+SDPA_F16, SDPA_BF16, SDPA_E4M3 = range(3)
+_DT = {torch.float16: SDPA_F16, torch.bfloat16: SDPA_BF16, torch.float8_e4m3fn: SDPA_E4M3}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SdpaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {sdpa_status_string(status)} ({status})")
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m flash_attention_forward_gb300.build` "
+                               f"(or __graft_entry__.build())")
+        lib = ctypes.CDLL(LIB_PATH)
+        p, i, i64, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+        lib.sdpa_fwd_workspace_size.argtypes = [i, i, i, i]
+        lib.sdpa_fwd_workspace_size.restype = sz
+        lib.sdpa_fwd.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, p, f, i, p, p, p, sz, i, i, p]
+        lib.sdpa_fwd.restype = i
+        lib.sdpa_fwd_fp8.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, p, f, i, p, p, p, sz, f, f, f, i, p]
+        lib.sdpa_fwd_fp8.restype = i
+        lib.sdpa_decode_workspace_size.argtypes = [i, i, i, i]
+        lib.sdpa_decode_workspace_size.restype = sz
+        lib.sdpa_decode.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, p, f, p, sz, i, p]
+        lib.sdpa_decode.restype = i
+        lib.sdpa_check_device_status.argtypes = [p]
+        lib.sdpa_check_device_status.restype = i
+        lib.sdpa_status_string.argtypes = [i]
+        lib.sdpa_status_string.restype = ctypes.c_char_p
+        lib.sdpa_version.argtypes = []
+        lib.sdpa_version.restype = i
+        _lib = lib
+        return lib
+
+
+def library():
+    """The loaded ctypes library (raises if it has not been built)."""
+    return _load()
+
+
+def declared_functions():
+    """Names of the functions include/sdpa.h declares."""
+    text = open(HEADER_PATH).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(sdpa_\w+)\s*\(", text, flags=re.M)))
+
+
+def sdpa_status_string(status: int) -> str:
+    return _load().sdpa_status_string(int(status)).decode()
+
+
+def sdpa_version() -> int:
+    return _load().sdpa_version()
+
+
+def _stream_ptr(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(name, rc):
+    if rc != SDPA_OK:
+        raise SdpaError(name, rc)
+
+
+def _i64(vals):
+    arr = (ctypes.c_int64 * len(vals))(*[int(x) for x in vals])
+    return arr
+
+
+def sdpa_fwd_workspace_size(B: int, Sq: int, Sk: int, has_mask: bool) -> int:
+    return int(_load().sdpa_fwd_workspace_size(B, Sq, Sk, int(bool(has_mask))))
+
+
+def sdpa_decode_workspace_size(B: int, Hq: int, max_kv: int, Dv: int) -> int:
+    return int(_load().sdpa_decode_workspace_size(B, Hq, max_kv, Dv))
+
+
+def _fwd_args(q, k, v, out, lse, mask, workspace, out_dtype, return_lse):
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, S, H, D]")
+    B, Sq, Hq, D = q.shape
+    _, Sk, Hkv, _ = k.shape
+    Dv = v.shape[-1]
+    for t in (q, k, v):
+        if not t.is_cuda or t.stride(-1) != 1:
+            raise ValueError("q, k, v must be CUDA tensors with unit innermost stride")
+    if out is None:
+        out = torch.empty((B, Sq, Hq, Dv), dtype=out_dtype, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    if lse is not None and (tuple(lse.shape) != (B, Hq, Sq) or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous fp32 [B, Hq, Sq] tensor")
+    strides = _i64([*q.stride()[:3], *k.stride()[:3], *v.stride()[:3], *out.stride()[:3]])
+    mstr = None
+    if mask is not None:
+        if mask.dtype != torch.float16 or mask.dim() != 3 or mask.stride(-1) != 1:
+            raise ValueError("mask must be an fp16 [B, Sq, Sk] tensor with unit innermost stride")
+        mstr = _i64([mask.stride(0), mask.stride(1)])
+        need = sdpa_fwd_workspace_size(B, Sq, Sk, True)
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return B, Sq, Hq, Hkv, Sk, D, Dv, out, lse, strides, mstr, workspace, ws_bytes
+
+
+def sdpa_fwd(q, k, v, *, scale: float | None = None, causal: bool = False, mask=None, out=None, lse=None,
+             return_lse: bool = True, workspace=None, stream=None):
+    """O = softmax(scale * Q K^T + mask) V for fp16/bf16 q [B,Sq,Hq,D], k [B,Sk,Hkv,D], v [B,Sk,Hkv,Dv].
+
+    Returns (o [B,Sq,Hq,Dv] in the input dtype, lse [B,Hq,Sq] fp32 or None)."""
+    if q.dtype not in (torch.float16, torch.bfloat16):
+        raise ValueError("sdpa_fwd takes fp16 or bf16 inputs (use sdpa_fwd_fp8 for e4m3)")
+    scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
+    B, Sq, Hq, Hkv, Sk, D, Dv, out, lse, strides, mstr, workspace, ws_bytes = _fwd_args(
+        q, k, v, out, lse, mask, workspace, q.dtype, return_lse)
+    rc = _load().sdpa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk, D, Dv, strides,
+                          scale, int(bool(causal)), _ptr(mask), mstr, _ptr(workspace), ws_bytes, _DT[q.dtype],
+                          _DT[out.dtype], _stream_ptr(stream))
+    _check("sdpa_fwd", rc)
+    return out, lse
+
+
+def sdpa_fwd_fp8(q, k, v, descale_q: float, descale_k: float, descale_v: float, *, scale: float | None = None,
+                 causal: bool = False, mask=None, out=None, lse=None, return_lse: bool = True, workspace=None,
+                 stream=None):
+    """e4m3 prefill: Q = q * descale_q (likewise K, V).  Returns (o bf16, lse fp32 or None)."""
+    if q.dtype != torch.float8_e4m3fn:
+        raise ValueError("sdpa_fwd_fp8 takes float8_e4m3fn inputs")
+    scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
+    B, Sq, Hq, Hkv, Sk, D, Dv, out, lse, strides, mstr, workspace, ws_bytes = _fwd_args(
+        q, k, v, out, lse, mask, workspace, torch.bfloat16, return_lse)
+    rc = _load().sdpa_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk, D, Dv, strides,
+                              scale, int(bool(causal)), _ptr(mask), mstr, _ptr(workspace), ws_bytes,
+                              float(descale_q), float(descale_k), float(descale_v), _DT[out.dtype],
+                              _stream_ptr(stream))
+    _check("sdpa_fwd_fp8", rc)
+    return out, lse
+
+
+def sdpa_decode(q, k_cache, v_cache, kv_len, *, scale: float | None = None, out=None, lse=None,
+                return_lse: bool = True, workspace=None, stream=None):
+    """Decode: q [B,Hq,D], caches [B,max_kv,Hkv,D|Dv], kv_len int32 [B] (device).  Returns (o, lse)."""
+    if q.dim() != 3 or k_cache.dim() != 4 or v_cache.dim() != 4:
+        raise ValueError("q must be [B, Hq, D], caches [B, max_kv, Hkv, D]")
+    B, Hq, D = q.shape
+    _, max_kv, Hkv, _ = k_cache.shape
+    Dv = v_cache.shape[-1]
+    if kv_len.dtype != torch.int32 or not kv_len.is_cuda:
+        raise ValueError("kv_len must be an int32 CUDA tensor")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty((B, Hq, Dv), dtype=q.dtype, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    need = sdpa_decode_workspace_size(B, Hq, max_kv, Dv)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    strides = _i64([*q.stride()[:2], *k_cache.stride()[:3], *v_cache.stride()[:3], *out.stride()[:2]])
+    rc = _load().sdpa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), _ptr(out), _ptr(lse), B, Hq,
+                             Hkv, max_kv, D, Dv, strides, scale, _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _DT[q.dtype], _stream_ptr(stream))
+    _check("sdpa_decode", rc)
+    return out, lse
+
+
+def sdpa_check_device_status(stream=None) -> int:
+    """Synchronizes the stream and returns (and clears) the device status (SDPA_OK if clean)."""
+    return int(_load().sdpa_check_device_status(_stream_ptr(stream)))

@@ -1,0 +1,288 @@
+// C ABI of the library (declared in include/sdpa.h): argument validation, tensor-map
+// encoding, instance dispatch and the device status word.  No entry point allocates
+// device memory; every argument is checked before the first CUDA call.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/sdpa.h"
+#include "internal.h"
+
+namespace sdpa {
+namespace {
+
+__device__ uint32_t g_status_word;
+
+constexpr int kMaxDevices = 64;
+uint32_t* g_status_ptr[kMaxDevices] = {};
+std::mutex g_mu;
+
+// Device address of this device's status word (looked up once per device).
+cudaError_t status_ptr(uint32_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_status_word);
+    if (e != cudaSuccess) return e;
+    g_status_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return cudaSuccess;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Tensor map of a [B, S, H, Dh] tensor (element strides sb, ss, sh; innermost stride 1),
+// box = box0 x 1 x box_rows x 1.
+bool encode_bshd(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int esize, int B, int S, int H, int Dh,
+                 int64_t sb, int64_t ss, int64_t sh, int box0, int box_rows, CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)Dh, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)(sh * esize), (cuuint64_t)(ss * esize), (cuuint64_t)(sb * esize)};
+  const cuuint32_t box[4] = {(cuuint32_t)box0, 1u, (cuuint32_t)box_rows, 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  return fn(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Strides usable by a tensor map / 16-byte vector access: positive multiples of `mult` (a
+// stride of a size-1 dimension only needs the multiple).
+bool stride_ok(int64_t s, int64_t mult) { return s >= 0 && s % mult == 0 && s < (int64_t(1) << 36); }
+
+size_t round16(size_t x) { return (x + 15) & ~size_t(15); }
+
+size_t mask_ws_bytes(int B, int Sq, int Sk) {
+  const size_t nkb = (size_t)((Sk + kBlockK - 1) / kBlockK);
+  const size_t rows = (size_t)B * (size_t)Sq;
+  return round16(rows * nkb * sizeof(uint4)) + round16(rows * nkb);
+}
+
+int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,
+               int Sk, int D, int Dv, const int64_t* strides, float scale, int causal, const void* mask,
+               const int64_t* mask_strides, void* workspace, size_t workspace_bytes, int elem, float descale_q,
+               float descale_k, float descale_v, sdpa_dtype out_dtype, void* stream) {
+  // ---- validation (no CUDA call before this block passes)
+  if (!q || !k || !v || !o) return SDPA_ERR_INVALID;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Sk < 1 || D < 1 || Dv < 1) return SDPA_ERR_INVALID;
+  if (Hq % Hkv != 0) return SDPA_ERR_INVALID;
+  if (!(std::isfinite(scale) && scale > 0.f)) return SDPA_ERR_INVALID;
+  if (!(std::isfinite(descale_q) && descale_q > 0.f && std::isfinite(descale_k) && descale_k > 0.f &&
+        std::isfinite(descale_v) && descale_v > 0.f))
+    return SDPA_ERR_INVALID;
+  const int esize = (elem == kE4M3) ? 1 : 2;
+  if (elem == kE4M3) {
+    if (!((D == 128 && Dv == 128) || (D == 192 && Dv == 128))) return SDPA_ERR_UNSUPPORTED;
+    if (out_dtype != SDPA_BF16) return SDPA_ERR_UNSUPPORTED;
+  } else {
+    if (!((D == 64 && Dv == 64) || (D == 128 && Dv == 128))) return SDPA_ERR_UNSUPPORTED;
+    if ((elem == kF16 && out_dtype != SDPA_F16) || (elem == kBF16 && out_dtype != SDPA_BF16))
+      return SDPA_ERR_UNSUPPORTED;
+  }
+  int64_t st[SDPA_FWD_NSTRIDES];
+  if (strides) {
+    std::memcpy(st, strides, sizeof(st));
+  } else {
+    const int64_t cs[SDPA_FWD_NSTRIDES] = {(int64_t)Sq * Hq * D,  (int64_t)Hq * D,  D,
+                                           (int64_t)Sk * Hkv * D, (int64_t)Hkv * D, D,
+                                           (int64_t)Sk * Hkv * Dv, (int64_t)Hkv * Dv, Dv,
+                                           (int64_t)Sq * Hq * Dv, (int64_t)Hq * Dv, Dv};
+    std::memcpy(st, cs, sizeof(st));
+  }
+  const int64_t in_mult = 16 / esize;  // 16-byte tensor-map strides
+  for (int i = 0; i < 9; ++i)
+    if (!stride_ok(st[i], in_mult)) return SDPA_ERR_UNSUPPORTED;
+  for (int i = 9; i < 12; ++i)
+    if (!stride_ok(st[i], 8)) return SDPA_ERR_UNSUPPORTED;  // 16-byte output vectors
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return SDPA_ERR_UNSUPPORTED;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SDPA_ERR_INVALID;
+  const int n_kblocks = (Sk + kBlockK - 1) / kBlockK;
+  const int n_cta_tiles = (Sq + kCtaRows - 1) / kCtaRows;
+  if ((long long)n_cta_tiles * B * Hq >= (1ll << 31)) return SDPA_ERR_UNSUPPORTED;
+  int64_t mb = 0, mi = 0;
+  if (mask) {
+    if (reinterpret_cast<uintptr_t>(mask) & 1u) return SDPA_ERR_INVALID;
+    mb = mask_strides ? mask_strides[0] : (int64_t)Sq * Sk;
+    mi = mask_strides ? mask_strides[1] : (int64_t)Sk;
+    if (mb < 0 || mi < 0) return SDPA_ERR_INVALID;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < mask_ws_bytes(B, Sq, Sk)) return SDPA_ERR_INVALID;
+  }
+
+  // ---- tensor maps
+  const CUtensorMapDataType dt = elem == kE4M3   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : elem == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapSwizzle sw_qk = elem == kE4M3 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+  alignas(64) CUtensorMap tq, tk, tv;
+  if (!encode_bshd(&tq, q, dt, esize, B, Sq, Hq, D, st[0], st[1], st[2], 64, kBlockQ, sw_qk)) return SDPA_ERR_CUDA;
+  if (!encode_bshd(&tk, k, dt, esize, B, Sk, Hkv, D, st[3], st[4], st[5], 64, kBlockK, sw_qk)) return SDPA_ERR_CUDA;
+  const bool v_ok = elem == kE4M3
+                        ? encode_bshd(&tv, v, dt, 1, B, Sk, Hkv, Dv, st[6], st[7], st[8], Dv, kBlockK,
+                                      CU_TENSOR_MAP_SWIZZLE_NONE)
+                        : encode_bshd(&tv, v, dt, 2, B, Sk, Hkv, Dv, st[6], st[7], st[8], 64, kBlockK,
+                                      CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!v_ok) return SDPA_ERR_CUDA;
+
+  uint32_t* status = nullptr;
+  if (status_ptr(&status) != cudaSuccess) return SDPA_ERR_CUDA;
+  cudaStream_t stm = static_cast<cudaStream_t>(stream);
+
+  PrefillParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.o_b = st[9], p.o_s = st[10], p.o_h = st[11];
+  p.B = B, p.Hq = Hq, p.Hkv = Hkv, p.Sq = Sq, p.Sk = Sk;
+  p.group = Hq / Hkv;
+  p.n_cta_tiles = n_cta_tiles;
+  p.n_kblocks = n_kblocks;
+  const double s_eff = (double)scale * (double)descale_q * (double)descale_k;
+  p.scale2 = (float)(s_eff * 1.4426950408889634);
+  p.inv_scale = (float)(1.0 / s_eff);
+  p.out_scale = descale_v;
+  p.status = status;
+  if (mask) {
+    const size_t rows = (size_t)B * (size_t)Sq;
+    uint4* bits = static_cast<uint4*>(workspace);
+    uint8_t* flags = reinterpret_cast<uint8_t*>(static_cast<char*>(workspace) + round16(rows * n_kblocks * sizeof(uint4)));
+    MaskConvertParams mp{static_cast<const uint16_t*>(mask), mb, mi, B, Sq, Sk, n_kblocks, bits, flags};
+    if (launch_mask_convert(mp, stm) != cudaSuccess) return SDPA_ERR_CUDA;
+    p.mask_bits = bits;
+    p.mask_flags = flags;
+    p.mask = static_cast<const uint16_t*>(mask);
+    p.mask_b = mb, p.mask_i = mi;
+  }
+  bool supported = false;
+  cudaError_t e;
+  if (elem == kE4M3)
+    e = launch_prefill_e4m3(D, Dv, causal != 0, mask != nullptr, tq, tk, tv, p, stm, &supported);
+  else if (elem == kBF16)
+    e = launch_prefill_bf16(D, Dv, causal != 0, mask != nullptr, tq, tk, tv, p, stm, &supported);
+  else
+    e = launch_prefill_f16(D, Dv, causal != 0, mask != nullptr, tq, tk, tv, p, stm, &supported);
+  if (!supported) return SDPA_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace sdpa
+
+using namespace sdpa;
+
+extern "C" {
+
+size_t sdpa_fwd_workspace_size(int B, int Sq, int Sk, int has_mask) {
+  if (!has_mask || B < 1 || Sq < 1 || Sk < 1) return 0;
+  return mask_ws_bytes(B, Sq, Sk);
+}
+
+int sdpa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,
+             int Sk, int D, int Dv, const int64_t* strides, float scale, int causal, const void* mask,
+             const int64_t* mask_strides, void* workspace, size_t workspace_bytes, sdpa_dtype in_dtype,
+             sdpa_dtype out_dtype, void* stream) {
+  if (in_dtype != SDPA_F16 && in_dtype != SDPA_BF16) return SDPA_ERR_UNSUPPORTED;
+  return fwd_common(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, Dv, strides, scale, causal, mask, mask_strides,
+                    workspace, workspace_bytes, in_dtype == SDPA_BF16 ? kBF16 : kF16, 1.f, 1.f, 1.f, out_dtype,
+                    stream);
+}
+
+int sdpa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,
+                 int Sk, int D, int Dv, const int64_t* strides, float scale, int causal, const void* mask,
+                 const int64_t* mask_strides, void* workspace, size_t workspace_bytes, float descale_q,
+                 float descale_k, float descale_v, sdpa_dtype out_dtype, void* stream) {
+  return fwd_common(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, Dv, strides, scale, causal, mask, mask_strides,
+                    workspace, workspace_bytes, kE4M3, descale_q, descale_k, descale_v, out_dtype, stream);
+}
+
+size_t sdpa_decode_workspace_size(int B, int Hq, int max_kv, int Dv) {
+  if (B < 1 || Hq < 1 || max_kv < 1 || Dv < 1) return 0;
+  const size_t n_splits = (size_t)((max_kv + kDecodeSplit - 1) / kDecodeSplit);
+  return round16((size_t)B * Hq * n_splits * (size_t)(Dv + 2) * sizeof(float));
+}
+
+int sdpa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_len, void* o, float* lse,
+                int B, int Hq, int Hkv, int max_kv, int D, int Dv, const int64_t* strides, float scale,
+                void* workspace, size_t workspace_bytes, sdpa_dtype dtype, void* stream) {
+  if (!q || !k_cache || !v_cache || !kv_len || !o) return SDPA_ERR_INVALID;
+  if (B < 1 || Hq < 1 || Hkv < 1 || max_kv < 1 || D < 1 || Dv < 1) return SDPA_ERR_INVALID;
+  if (Hq % Hkv != 0) return SDPA_ERR_INVALID;
+  if (!(std::isfinite(scale) && scale > 0.f)) return SDPA_ERR_INVALID;
+  if (dtype != SDPA_F16 && dtype != SDPA_BF16) return SDPA_ERR_UNSUPPORTED;
+  if (D != 128 || Dv != kDecodeDv) return SDPA_ERR_UNSUPPORTED;
+  const int group = Hq / Hkv;
+  if (group > 8) return SDPA_ERR_UNSUPPORTED;
+  if (B > 65535 || Hkv > 65535) return SDPA_ERR_UNSUPPORTED;
+  int64_t st[SDPA_DECODE_NSTRIDES];
+  if (strides) {
+    std::memcpy(st, strides, sizeof(st));
+  } else {
+    const int64_t cs[SDPA_DECODE_NSTRIDES] = {(int64_t)Hq * D, D, (int64_t)max_kv * Hkv * D, (int64_t)Hkv * D, D,
+                                              (int64_t)max_kv * Hkv * Dv, (int64_t)Hkv * Dv, Dv, (int64_t)Hq * Dv,
+                                              Dv};
+    std::memcpy(st, cs, sizeof(st));
+  }
+  for (int i = 0; i < SDPA_DECODE_NSTRIDES; ++i)
+    if (!stride_ok(st[i], 8)) return SDPA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o)) return SDPA_ERR_UNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(kv_len) & 3u) return SDPA_ERR_INVALID;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SDPA_ERR_INVALID;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < sdpa_decode_workspace_size(B, Hq, max_kv, Dv))
+    return SDPA_ERR_INVALID;
+
+  DecodeParams p{};
+  p.q = q, p.k = k_cache, p.v = v_cache, p.kv_len = kv_len, p.o = o, p.lse = lse;
+  p.ws = static_cast<float*>(workspace);
+  p.q_b = st[0], p.q_h = st[1], p.k_b = st[2], p.k_s = st[3], p.k_h = st[4];
+  p.v_b = st[5], p.v_s = st[6], p.v_h = st[7], p.o_b = st[8], p.o_h = st[9];
+  p.B = B, p.Hq = Hq, p.Hkv = Hkv, p.max_kv = max_kv, p.group = group;
+  p.n_splits_max = (max_kv + kDecodeSplit - 1) / kDecodeSplit;
+  p.scale2 = (float)((double)scale * 1.4426950408889634);
+  const cudaError_t e = launch_decode(dtype == SDPA_BF16 ? kBF16 : kF16, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
+int sdpa_check_device_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SDPA_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_status_word, sizeof(word)) != cudaSuccess) return SDPA_ERR_CUDA;
+  if (word == 0) return SDPA_OK;
+  const uint32_t zero = 0;
+  if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return SDPA_ERR_CUDA;
+  return (word & kStatusTimeout) ? SDPA_ERR_TIMEOUT : SDPA_ERR_CUDA;
+}
+
+const char* sdpa_status_string(int status) {
+  switch (status) {
+    case SDPA_OK: return "SDPA_OK";
+    case SDPA_ERR_INVALID: return "SDPA_ERR_INVALID";
+    case SDPA_ERR_UNSUPPORTED: return "SDPA_ERR_UNSUPPORTED";
+    case SDPA_ERR_CUDA: return "SDPA_ERR_CUDA";
+    case SDPA_ERR_TIMEOUT: return "SDPA_ERR_TIMEOUT";
+    default: return "SDPA_ERR_UNKNOWN";
+  }
+}
+
+int sdpa_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,82 @@
+// Host/device parameter blocks and the launch functions each kernel file exports to the
+// C-ABI layer.  Internal: not part of the public header.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace sdpa {
+
+// Status bits a kernel ORs into the device status word.
+enum : uint32_t { kStatusTimeout = 1u };
+
+// Prefill tile geometry shared by host and device.
+constexpr int kBlockQ = 128;           // query rows per tile (one TMEM lane each)
+constexpr int kTilesPerCta = 2;        // two query tiles per CTA share every K/V block
+constexpr int kCtaRows = kBlockQ * kTilesPerCta;
+constexpr int kBlockK = 128;           // keys per K/V block
+constexpr int kPrefillThreads = 384;   // 12 warps: load, MMA, 2 helpers, 2 x 4 softmax
+
+enum ElemKind : int { kF16 = 0, kBF16 = 1, kE4M3 = 2 };
+
+struct PrefillParams {
+  void* o;                 // [B, Sq, Hq, Dv] out dtype
+  float* lse;              // [B, Hq, Sq] or null
+  int64_t o_b, o_s, o_h;   // element strides of o
+  int B, Hq, Hkv, Sq, Sk;
+  int group;               // Hq / Hkv
+  int n_cta_tiles;         // ceil(Sq / kCtaRows)
+  int n_kblocks;           // ceil(Sk / kBlockK)
+  float scale2;            // scale * log2(e) (times descale_q * descale_k for e4m3)
+  float inv_scale;         // 1 / (scale * descale_q * descale_k): mask values enter s in score units
+  float out_scale;         // descale_v for e4m3, else 1
+  // condensed additive mask (null when there is none)
+  const uint4* mask_bits;  // [B, Sq, n_kblocks] x 128 bits, bit set = -inf
+  const uint8_t* mask_flags;  // [B, Sq, n_kblocks], 1 = block row holds finite non-zero values
+  const uint16_t* mask;    // original fp16 mask, read only for flagged block rows
+  int64_t mask_b, mask_i;  // element strides of the original mask
+  uint32_t* status;        // device status word
+};
+
+struct DecodeParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  const int32_t* kv_len;
+  void* o;
+  float* lse;
+  float* ws;               // [B, Hq, n_splits_max, Dv + 2]
+  int64_t q_b, q_h, k_b, k_s, k_h, v_b, v_s, v_h, o_b, o_h;
+  int B, Hq, Hkv, max_kv, group, n_splits_max;
+  float scale2;            // scale * log2(e)
+};
+
+constexpr int kDecodeSplit = 1024;      // keys per phase-1 CTA
+constexpr int kDecodeWarps = 4;         // each warp streams kDecodeSplit / kDecodeWarps keys
+constexpr int kDecodeDv = 128;
+
+struct MaskConvertParams {
+  const uint16_t* mask;
+  int64_t mask_b, mask_i;
+  int B, Sq, Sk, n_kblocks;
+  uint4* bits;
+  uint8_t* flags;
+};
+
+// Kernel launchers (return cudaError_t of the launch).  The prefill launchers set
+// *supported = false (and launch nothing) for head dims they were not built for.
+cudaError_t launch_prefill_f16(int D, int Dv, bool causal, bool has_mask, const CUtensorMap& tq,
+                               const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st,
+                               bool* supported);
+cudaError_t launch_prefill_bf16(int D, int Dv, bool causal, bool has_mask, const CUtensorMap& tq,
+                                const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st,
+                                bool* supported);
+cudaError_t launch_prefill_e4m3(int D, int Dv, bool causal, bool has_mask, const CUtensorMap& tq,
+                                const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st,
+                                bool* supported);
+cudaError_t launch_decode(int elem, const DecodeParams& p, cudaStream_t st);
+cudaError_t launch_mask_convert(const MaskConvertParams& p, cudaStream_t st);
+
+}  // namespace sdpa

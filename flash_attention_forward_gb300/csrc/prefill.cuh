@@ -1,0 +1,527 @@
+// Fused attention prefill for sm_103a: TMA -> shared-memory ring -> tcgen05 MMAs with
+// accumulators in tensor memory -> blocked online softmax -> P.V, warp-specialised.
+//
+// The algorithm is the blocked online softmax of the page "Xe SDPA Forward Mainloop"
+// (sections "mainloop_body(K)", "softmax() helper" and "Full simplified pseudocode"):
+// per K/V block, S = Q K^T accumulated over the head dim, mask, new row max, rescale of
+// the running O and l, P = exp2(scale*log2(e)*S - max), l += rowsum(P), O += P V.  What is
+// laid out differently for this GPU:
+//   * one CTA owns two 128-row query tiles that share every K/V block; each tile has its
+//     own 128-column S and O accumulators in tensor memory (4 x 128 = 512 columns);
+//   * one thread issues every tcgen05.mma; the two softmax warpgroups ping-pong, so the
+//     tensor core works on one tile while the other tile's softmax runs;
+//   * P overwrites its own S columns in tensor memory (16-bit, packed in pairs) and feeds
+//     the P.V MMA directly from there;
+//   * the O rescale is lazy: the stale row max is kept until the max grows by more than
+//     kRescaleLog2 (log2 units), which is exact because O and l always share the max;
+//   * masking touches only the blocks that need it (the causal diagonal and the ragged
+//     last block); fully hidden causal blocks are never loaded.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace sdpa {
+
+constexpr float kRescaleLog2 = 8.0f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int ELEM, int D, int DV>
+struct PrefillCfg {
+  static constexpr int ESZ = (ELEM == kE4M3) ? 1 : 2;
+  static constexpr int CH = 64;                 // elements per swizzle chunk (TMA box width)
+  static constexpr int CHB = CH * ESZ;          // 128 B (16-bit) or 64 B (e4m3)
+  static constexpr uint32_t SW = (CHB == 128) ? kSwizzle128B : kSwizzle64B;
+  static constexpr int NCH_D = D / CH;
+  static constexpr int NCH_V = DV / 64;         // V is always 16-bit in shared memory
+  static constexpr int STAGES = (D <= 64) ? 4 : 2;
+  static constexpr int Q_BYTES = kBlockQ * D * ESZ;
+  static constexpr int K_BYTES = kBlockK * D * ESZ;
+  static constexpr int V_BYTES = kBlockK * DV * 2;
+  static constexpr int VRAW_BYTES = (ELEM == kE4M3) ? kBlockK * DV : 0;
+  static constexpr int KSTEP_BYTES = 32;        // K extent of one MMA: 16 x 16-bit or 32 x e4m3
+  static constexpr int STEPS_PER_CH = CHB / KSTEP_BYTES;
+  static constexpr int QK_STEPS = D * ESZ / KSTEP_BYTES;
+  static constexpr int PV_STEPS = kBlockK / 16;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + kTilesPerCta * Q_BYTES;
+  static constexpr int OFF_V = OFF_K + STAGES * K_BYTES;
+  static constexpr int OFF_VRAW = OFF_V + STAGES * V_BYTES;
+  static constexpr int OFF_BAR = OFF_VRAW + STAGES * VRAW_BYTES;
+  // barriers, tmem base, abort flag; then 1 KB of slack so that the 1024-B alignment of the
+  // dynamic shared window never pushes the last byte past the allocation
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;
+  static_assert(D % CH == 0 && DV % 64 == 0, "head dims must be multiples of 64");
+  static_assert(Q_BYTES % 1024 == 0 && K_BYTES % 1024 == 0 && V_BYTES % 1024 == 0, "1 KB tile alignment");
+};
+
+template <int ELEM>
+struct ElemTraits;
+template <>
+struct ElemTraits<kF16> {
+  static constexpr uint32_t qk_fmt = 0, pv_fmt = 0;  // f16 x f16, P f16
+};
+template <>
+struct ElemTraits<kBF16> {
+  static constexpr uint32_t qk_fmt = 1, pv_fmt = 1;  // bf16 x bf16, P bf16
+};
+template <>
+struct ElemTraits<kE4M3> {
+  static constexpr uint32_t qk_fmt = 0, pv_fmt = 0;  // e4m3 x e4m3 (kind::f8f6f4), P and V f16
+};
+
+template <int ELEM>
+__device__ __forceinline__ uint32_t pack_p(float lo, float hi) {
+  if constexpr (ELEM == kBF16)
+    return pack_bf16x2(lo, hi);
+  else
+    return pack_f16x2(lo, hi);
+}
+
+template <int ELEM>
+__device__ __forceinline__ float p_lo(uint32_t w) {
+  if constexpr (ELEM == kBF16)
+    return bf16lo_f32(w);
+  else
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu)));
+}
+
+template <int ELEM>
+__device__ __forceinline__ float p_hi(uint32_t w) {
+  if constexpr (ELEM == kBF16)
+    return bf16hi_f32(w);
+  else
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+}
+
+// Output element packing (bf16 unless the inputs are f16).
+template <int ELEM>
+__device__ __forceinline__ uint32_t pack_out(float lo, float hi) {
+  if constexpr (ELEM == kF16)
+    return pack_f16x2(lo, hi);
+  else
+    return pack_bf16x2(lo, hi);
+}
+
+// Eight e4m3 codes (two 32-bit words) -> eight f16 values (four f16x2 words); exact.
+__device__ __forceinline__ uint4 e4m3x8_to_f16x8(uint2 in) {
+  uint4 out;
+  asm("{\n\t.reg .b16 a, b, c, d;\n\t"
+      "mov.b32 {a, b}, %4;\n\t"
+      "mov.b32 {c, d}, %5;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, b;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %2, c;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %3, d;\n\t}"
+      : "=r"(out.x), "=r"(out.y), "=r"(out.z), "=r"(out.w)
+      : "r"(in.x), "r"(in.y));
+  return out;
+}
+
+struct CtaWork {
+  int b, h, kvh, q0;
+  int n_t[kTilesPerCta];  // K/V blocks each query tile needs (0 = tile entirely past Sq)
+  int n_blocks;           // blocks streamed for the CTA = max over tiles
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ CtaWork cta_work(const PrefillParams& p) {
+  CtaWork w;
+  const int bh_count = p.B * p.Hq;
+  const int lin = blockIdx.x;
+  const int bh = lin % bh_count;
+  const int rank = lin / bh_count;
+  // causal tiles at the bottom of the matrix see the most keys: launch them first
+  const int ctile = CAUSAL ? (p.n_cta_tiles - 1 - rank) : rank;
+  w.b = bh / p.Hq;
+  w.h = bh % p.Hq;
+  w.kvh = w.h / p.group;
+  w.q0 = ctile * kCtaRows;
+  w.n_blocks = 0;
+#pragma unroll
+  for (int t = 0; t < kTilesPerCta; ++t) {
+    const int r0 = w.q0 + t * kBlockQ;
+    int n = 0;
+    if (r0 < p.Sq) {
+      n = p.n_kblocks;
+      if (CAUSAL) {
+        const int last_row = min(r0 + kBlockQ - 1, p.Sq - 1);
+        n = min(n, last_row / kBlockK + 1);
+      }
+    }
+    w.n_t[t] = n;
+    w.n_blocks = max(w.n_blocks, n);
+  }
+  return w;
+}
+
+template <int ELEM, int D, int DV, bool CAUSAL, bool MASK>
+__global__ void __launch_bounds__(kPrefillThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+  using C = PrefillCfg<ELEM, D, DV>;
+  constexpr int ST = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + C::OFF_Q;
+  uint8_t* sK = smem + C::OFF_K;
+  uint8_t* sV = smem + C::OFF_V;
+  uint8_t* sVraw = smem + C::OFF_VRAW;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bars;                 // [2]
+  uint64_t* kv_full = q_full + 2;          // [ST]
+  uint64_t* kv_empty = kv_full + ST;       // [ST]
+  uint64_t* v_ready = kv_empty + ST;       // [ST] (e4m3: converted V ready)
+  uint64_t* s_full = v_ready + ST;         // [2]
+  uint64_t* p_full = s_full + 2;           // [2]
+  uint64_t* o_done = p_full + 2;           // [2]
+  uint64_t* mma_done = o_done + 2;         // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const CtaWork w = cta_work<CAUSAL>(p);
+
+  if (tid == 0) {
+    mbar_init(&q_full[0], 1);
+    mbar_init(&q_full[1], 1);
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+      mbar_init(&v_ready[s], 64);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 128);
+      mbar_init(&o_done[t], 1);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      for (int t = 0; t < kTilesPerCta; ++t) {
+        if (w.n_t[t] == 0) continue;
+        mbar_arrive_expect_tx(&q_full[t], C::Q_BYTES);
+        for (int c = 0; c < C::NCH_D; ++c)
+          tma_load_4d(sQ + t * C::Q_BYTES + c * kBlockQ * C::CHB, &tm_q, &q_full[t], c * C::CH, w.h,
+                      w.q0 + t * kBlockQ, w.b);
+      }
+      int issued = 0;
+      for (int j = 0; j < w.n_blocks; ++j) {
+        const int s = j % ST;
+        const int r = j / ST;
+        if (r > 0 && !mbar_wait(&kv_empty[s], (r - 1) & 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(&kv_full[s], C::K_BYTES + (ELEM == kE4M3 ? C::VRAW_BYTES : C::V_BYTES));
+        for (int c = 0; c < C::NCH_D; ++c)
+          tma_load_4d(sK + s * C::K_BYTES + c * kBlockK * C::CHB, &tm_k, &kv_full[s], c * C::CH, w.kvh,
+                      j * kBlockK, w.b);
+        if constexpr (ELEM == kE4M3) {
+          tma_load_4d(sVraw + s * C::VRAW_BYTES, &tm_v, &kv_full[s], 0, w.kvh, j * kBlockK, w.b);
+        } else {
+          for (int c = 0; c < C::NCH_V; ++c)
+            tma_load_4d(sV + s * C::V_BYTES + c * kBlockK * 128, &tm_v, &kv_full[s], c * 64, w.kvh, j * kBlockK,
+                        w.b);
+        }
+        issued = j + 1;
+      }
+      if (*abort_flag) {
+        // let every copy already in flight land before the CTA's shared memory goes away
+        for (int t = 0; t < kTilesPerCta; ++t)
+          if (w.n_t[t] > 0) mbar_drain(&q_full[t], 0);
+        for (int j = max(0, issued - ST); j < issued; ++j) mbar_drain(&kv_full[j % ST], (j / ST) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (one thread)
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk =
+          make_idesc(ElemTraits<ELEM>::qk_fmt, ElemTraits<ELEM>::qk_fmt, 0, 0, kBlockQ, kBlockK);
+      constexpr uint32_t idesc_pv = make_idesc(ElemTraits<ELEM>::pv_fmt, ElemTraits<ELEM>::pv_fmt, 0, 1, kBlockQ, DV);
+      const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
+      bool ok = true;
+      for (int t = 0; t < kTilesPerCta && ok; ++t)
+        if (w.n_t[t] > 0) ok = mbar_wait(&q_full[t], 0, abort_flag, p.status);
+      for (int j = 0; ok && j <= w.n_blocks; ++j) {
+        const int s = j % ST, r = j / ST;
+        const int sp = (j + ST - 1) % ST, rp = (j - 1) / ST;  // stage / round of block j-1
+        bool k_ready = false;
+        if (ELEM == kE4M3 && j >= 1) {
+          if (!mbar_wait(&v_ready[sp], rp & 1, abort_flag, p.status)) break;
+        }
+        for (int t = 0; t < kTilesPerCta; ++t) {
+          const uint32_t tS = tmem_base + t * 128;
+          const uint32_t tO = tmem_base + 256 + t * 128;
+          // O_t += P_t(j-1) V(j-1), with P read from tensor memory
+          if (j >= 1 && j - 1 < w.n_t[t]) {
+            if (!mbar_wait(&p_full[t], (j - 1) & 1, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < C::PV_STEPS; ++kk) {
+              const uint64_t bdesc =
+                  make_smem_desc(sVa + sp * C::V_BYTES + kk * 16 * 128, kBlockK * 128, 1024, kSwizzle128B);
+              mma_f16_ts(tO, tS + kk * 8, bdesc, idesc_pv, (j - 1 > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&o_done[t]);
+          }
+          // block j-1 is no longer needed once the MMAs issued so far complete
+          if (t == kTilesPerCta - 1 && j >= 1) mma_commit(&kv_empty[sp]);
+          // S_t = Q_t K(j)^T
+          if (j < w.n_t[t]) {
+            if (!k_ready) {
+              if (!mbar_wait(&kv_full[s], r & 1, abort_flag, p.status)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              k_ready = true;
+            }
+#pragma unroll
+            for (int kk = 0; kk < C::QK_STEPS; ++kk) {
+              const int ch = kk / C::STEPS_PER_CH;
+              const uint32_t off = ch * kBlockQ * C::CHB + (kk % C::STEPS_PER_CH) * C::KSTEP_BYTES;
+              const uint64_t adesc = make_smem_desc(sQa + t * C::Q_BYTES + off, 16, 8 * C::CHB, C::SW);
+              const uint64_t bdesc = make_smem_desc(sKa + s * C::K_BYTES + off, 16, 8 * C::CHB, C::SW);
+              if constexpr (ELEM == kE4M3)
+                mma_f8_ss(tS, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+              else
+                mma_f16_ss(tS, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&s_full[t]);
+          }
+        }
+      }
+      // every MMA issued so far has finished before tensor memory is released
+      mma_commit(mma_done);
+      mbar_drain(mma_done, 0);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ e4m3 V -> f16 converter
+    if constexpr (ELEM == kE4M3) {
+      const int ct = tid - 64;  // 0..63
+      for (int j = 0; j < w.n_blocks; ++j) {
+        const int s = j % ST, r = j / ST;
+        if (!mbar_wait(&kv_full[s], r & 1, abort_flag, p.status)) break;
+        const uint8_t* src = sVraw + s * C::VRAW_BYTES;
+        uint8_t* dst = sV + s * C::V_BYTES;
+        constexpr int UNITS = kBlockK * DV / 8;  // 8 values per unit
+#pragma unroll 4
+        for (int u = ct; u < UNITS; u += 64) {
+          const int row = u / (DV / 8), du = u % (DV / 8);
+          const int ch = du >> 3, uc = du & 7;
+          const uint2 raw = *reinterpret_cast<const uint2*>(src + row * DV + du * 8);
+          *reinterpret_cast<uint4*>(dst + ch * kBlockK * 128 + row * 128 + ((uc ^ (row & 7)) << 4)) =
+              e4m3x8_to_f16x8(raw);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&v_ready[s]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warpgroups
+    const int t = (warp - 4) >> 2;           // query tile of this warpgroup
+    const int wq = warp & 3;                 // tensor-memory lane quarter
+    const int row = wq * 32 + lane;          // row within the tile
+    const int qrow = w.q0 + t * kBlockQ + row;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem_base + lane_off + t * 128;
+    const uint32_t tO = tmem_base + lane_off + 256 + t * 128;
+    const int n = w.n_t[t];
+    const float scale2 = p.scale2;
+    float m_used = -INFINITY;
+    float l = 0.f;
+    bool ok = true;
+    const bool row_valid = qrow < p.Sq;
+    const uint4* bits_row = nullptr;
+    const uint8_t* flags_row = nullptr;
+    if constexpr (MASK) {
+      const int qr = row_valid ? qrow : 0;
+      bits_row = p.mask_bits + (static_cast<int64_t>(w.b) * p.Sq + qr) * p.n_kblocks;
+      flags_row = p.mask_flags + (static_cast<int64_t>(w.b) * p.Sq + qr) * p.n_kblocks;
+    }
+
+    for (int j = 0; j < n; ++j) {
+      uint4 mbits = make_uint4(0u, 0u, 0u, 0u);
+      uint32_t mflag = 0;
+      if constexpr (MASK) {
+        if (row_valid) {
+          mbits = __ldg(bits_row + j);
+          mflag = __ldg(flags_row + j);
+        }
+      }
+      if (!mbar_wait_warp(&s_full[t], j & 1, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[kBlockK];
+      {
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        tmem_ld32(tS + 0, r0);
+        tmem_ld32(tS + 32, r1);
+        tmem_ld32(tS + 64, r2);
+        tmem_ld32(tS + 96, r3);
+        tmem_ld_wait();
+        reg_fence(r0);
+        reg_fence(r1);
+        reg_fence(r2);
+        reg_fence(r3);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          s[c] = __uint_as_float(r0[c]);
+          s[32 + c] = __uint_as_float(r1[c]);
+          s[64 + c] = __uint_as_float(r2[c]);
+          s[96 + c] = __uint_as_float(r3[c]);
+        }
+      }
+      // the causal diagonal and the ragged last block: hide keys past the row / past Sk
+      const int k0 = j * kBlockK;
+      const bool edge = (CAUSAL && (k0 + kBlockK - 1 > w.q0 + t * kBlockQ)) || (k0 + kBlockK > p.Sk);
+      if (edge) {
+        const int lim = (CAUSAL ? min(p.Sk, qrow + 1) : p.Sk) - k0;
+#pragma unroll
+        for (int c = 0; c < kBlockK; ++c)
+          if (c >= lim) s[c] = -INFINITY;
+      }
+      if constexpr (MASK) {
+        if (mflag) {
+          // block row with finite non-zero mask values: add them (rare path)
+          const uint16_t* mrow = p.mask + static_cast<int64_t>(w.b) * p.mask_b + static_cast<int64_t>(qrow) * p.mask_i;
+#pragma unroll
+          for (int c = 0; c < kBlockK; ++c) {
+            if (k0 + c < p.Sk) {
+              const float mv = __half2float(__ushort_as_half(__ldg(mrow + k0 + c)));
+              s[c] += mv * p.inv_scale;
+            }
+          }
+        }
+        __syncwarp();
+        const uint32_t mw[4] = {mbits.x, mbits.y, mbits.z, mbits.w};
+#pragma unroll
+        for (int c = 0; c < kBlockK; ++c)
+          if ((mw[c >> 5] >> (c & 31)) & 1u) s[c] = -INFINITY;
+      }
+      // block row max (scale2 > 0, so the max of s orders like the max of scale2 * s)
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+      for (int c = 8; c < kBlockK; c += 8)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], s[c + i]);
+      const float mb = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float m_cand = fmaxf(m_used, mb * scale2);
+      const bool need = m_cand > m_used + kRescaleLog2;
+      const bool rescale = __any_sync(0xffffffffu, need);
+      float alpha = 1.f;
+      if (rescale) {
+        alpha = (m_cand == -INFINITY) ? 1.f : ex2(m_used - m_cand);
+        l *= alpha;
+        m_used = m_cand;
+      }
+      // P = exp2(scale2 * s - m), rounded to 16 bits; l sums the rounded values
+      const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+#pragma unroll
+          for (int w2 = 0; w2 < 32; ++w2) {
+            const int c = half * 64 + 2 * w2;
+            const float p0 = ex2(fmaf(s[c], scale2, neg_m));
+            const float p1 = ex2(fmaf(s[c + 1], scale2, neg_m));
+            pk[w2] = pack_p<ELEM>(p0, p1);
+            ls[w2 & 3] += p_lo<ELEM>(pk[w2]) + p_hi<ELEM>(pk[w2]);
+          }
+          tmem_st32(tS + half * 32, pk);
+        }
+      }
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      if (rescale && j > 0) {
+        // O holds P.V of blocks < j at the old max: wait for that MMA, then scale it
+        if (!mbar_wait_warp(&o_done[t], (j - 1) & 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < DV / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_ld_wait();
+          reg_fence(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + c * 32, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&p_full[t]);
+    }
+
+    // ------------------------------------------------------------ epilogue: O / l, LSE
+    const bool go = __all_sync(0xffffffffu, ok && n > 0 && !*abort_flag);
+    if (go) {
+      if (mbar_wait_warp(&o_done[t], (n - 1) & 1, abort_flag, p.status)) {
+        tc_fence_after();
+        const float inv = (l > 0.f) ? p.out_scale / l : 0.f;
+        uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
+                        2 * (static_cast<int64_t>(w.b) * p.o_b + static_cast<int64_t>(qrow) * p.o_s +
+                             static_cast<int64_t>(w.h) * p.o_h);
+#pragma unroll 1
+        for (int c = 0; c < DV / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_ld_wait();
+          reg_fence(o);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_out<ELEM>(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+          if (row_valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 64);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+        if (p.lse != nullptr && row_valid)
+          p.lse[(static_cast<int64_t>(w.b) * p.Hq + w.h) * p.Sq + qrow] =
+              (l > 0.f) ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+}  // namespace sdpa

@@ -1,0 +1,16 @@
+// Prefill instances for e4m3 inputs: (D, Dv) in {(128, 128), (192, 128)} x causal x mask.
+#include "prefill_launch.cuh"
+
+namespace sdpa {
+
+cudaError_t launch_prefill_e4m3(int D, int Dv, bool causal, bool has_mask, const CUtensorMap& tq,
+                                const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st,
+                                bool* supported) {
+  *supported = true;
+  if (D == 128 && Dv == 128) return launch_prefill_dims<kE4M3, 128, 128>(causal, has_mask, tq, tk, tv, p, st);
+  if (D == 192 && Dv == 128) return launch_prefill_dims<kE4M3, 192, 128>(causal, has_mask, tq, tk, tv, p, st);
+  *supported = false;
+  return cudaSuccess;
+}
+
+}  // namespace sdpa

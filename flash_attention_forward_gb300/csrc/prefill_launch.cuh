@@ -1,0 +1,31 @@
+// Host-side launch of one prefill kernel instance.
+#pragma once
+
+#include "prefill.cuh"
+
+namespace sdpa {
+
+template <int ELEM, int D, int DV, bool CAUSAL, bool MASK>
+cudaError_t launch_prefill_instance(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                    const PrefillParams& p, cudaStream_t st) {
+  using C = PrefillCfg<ELEM, D, DV>;
+  auto kern = prefill_kernel<ELEM, D, DV, CAUSAL, MASK>;
+  // the shared-memory opt-in is per device; setting it again is harmless
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  const long long grid = (long long)p.n_cta_tiles * p.B * p.Hq;
+  kern<<<(unsigned)grid, kPrefillThreads, C::SMEM, st>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+template <int ELEM, int D, int DV>
+cudaError_t launch_prefill_dims(bool causal, bool has_mask, const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st) {
+  if (causal)
+    return has_mask ? launch_prefill_instance<ELEM, D, DV, true, true>(tq, tk, tv, p, st)
+                    : launch_prefill_instance<ELEM, D, DV, true, false>(tq, tk, tv, p, st);
+  return has_mask ? launch_prefill_instance<ELEM, D, DV, false, true>(tq, tk, tv, p, st)
+                  : launch_prefill_instance<ELEM, D, DV, false, false>(tq, tk, tv, p, st);
+}
+
+}  // namespace sdpa

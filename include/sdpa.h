@@ -1,0 +1,161 @@
+/*
+ * sdpa.h -- C ABI of the GB300 (sm_103a) scaled-dot-product-attention forward library.
+ *
+ * What every prefill entry point computes, per batch b, query head h and query row i
+ * (page "Xe SDPA Forward Mainloop", sections "Full simplified pseudocode" and
+ * "softmax() helper"; GQA head mapping from page "Xe2 ESIMD Flash Attention - SDP
+ * Prefill & Decode", section "GQA layout"):
+ *
+ *     kvh        = h / (Hq / Hkv)
+ *     s[j]       = scale * dot(Q[b,i,h,:], K[b,j,kvh,:]) + mask[b,i,j]      (mask optional)
+ *     s[j]       = -inf  if causal and j > i                                 (top-left causal)
+ *     O[b,i,h,:] = sum_j softmax(s)[j] * V[b,j,kvh,:]
+ *     LSE[b,h,i] = ln sum_j exp(s[j])
+ *
+ * computed block by block with the online softmax (row max m, rescale of the running O
+ * and l, exp2 with scale*log2(e) folded in, row sum l).  A row whose keys are all
+ * masked (every s[j] = -inf) yields O = 0 and LSE = -inf, never NaN (page "Xe2 ESIMD
+ * Flash Attention", section "Correctness testing", names that row as the usual NaN
+ * source).  K/V lengths need not be multiples of any block size (same page, section
+ * "kv_len alignment").
+ *
+ * Conventions shared by all entry points
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library never
+ *    frees or retains them.  Scalars and stride arrays are HOST values.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL is the
+ *    legacy default stream).  The return value reports argument validation and launch
+ *    errors only.  Errors detected on the device (a bounded wait that gave up) are
+ *    reported by sdpa_check_device_status().
+ *  - Element strides are in ELEMENTS, not bytes; the innermost (head-dim) stride is 1.
+ *  - Validation happens before any CUDA call; an invalid call launches nothing.
+ *  - The library allocates no device memory in these entry points.  Decode and masked
+ *    prefill take a caller workspace sized by the *_workspace_size functions.
+ */
+#ifndef SDPA_GB300_H
+#define SDPA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SDPA_OK = 0,
+  SDPA_ERR_INVALID = 1,     /* bad argument: null pointer, non-positive size, Hq % Hkv != 0, bad scale */
+  SDPA_ERR_UNSUPPORTED = 2, /* valid but not built: head dims, dtypes, alignment, strides */
+  SDPA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (launch, tensor-map encode) */
+  SDPA_ERR_TIMEOUT = 4      /* a kernel's bounded wait gave up (see sdpa_check_device_status) */
+} sdpa_status;
+
+typedef enum { SDPA_F16 = 0, SDPA_BF16 = 1, SDPA_E4M3 = 2 } sdpa_dtype;
+
+/* Number of int64 entries in the prefill stride array. */
+#define SDPA_FWD_NSTRIDES 12
+/* Number of int64 entries in the decode stride array. */
+#define SDPA_DECODE_NSTRIDES 10
+
+/*
+ * sdpa_fwd_workspace_size -- bytes of device scratch sdpa_fwd / sdpa_fwd_fp8 need.
+ * Zero when has_mask == 0.  With an additive mask the library first condenses it into
+ * one bit per (row, key) marking -inf entries plus one flag per (row, 128-key block)
+ * marking blocks that hold finite non-zero values; this is that buffer.
+ */
+size_t sdpa_fwd_workspace_size(int B, int Sq, int Sk, int has_mask);
+
+/*
+ * sdpa_fwd -- fused attention prefill, fp16 or bf16 inputs, fp32 softmax state.
+ *
+ *   q    [B, Sq, Hq, D]      in_dtype         k [B, Sk, Hkv, D]   in_dtype
+ *   v    [B, Sk, Hkv, Dv]    in_dtype         o [B, Sq, Hq, Dv]   out_dtype (written)
+ *   lse  [B, Hq, Sq] fp32 contiguous, natural log; may be NULL (then not written)
+ *   strides: NULL for the contiguous layouts above, else 12 element strides
+ *            {q_b, q_s, q_h,  k_b, k_s, k_h,  v_b, v_s, v_h,  o_b, o_s, o_h}
+ *   scale:   > 0 and finite (the softmax temperature; 1/sqrt(D) is customary)
+ *   causal:  nonzero -> key j visible to query i iff j <= i (top-left aligned)
+ *   mask:    NULL, or fp16 additive mask indexed [b, i, j], shared by all heads, added
+ *            after scaling; element strides mask_strides = {m_b, m_i} (NULL means
+ *            {Sq*Sk, Sk}; m_b may be 0 to broadcast over the batch).  Only 2-byte
+ *            alignment is required.
+ *   workspace: device scratch of at least sdpa_fwd_workspace_size(B, Sq, Sk, mask!=0)
+ *            bytes, 16-byte aligned; may be NULL when mask is NULL.
+ *   in_dtype: SDPA_F16 or SDPA_BF16.  out_dtype: SDPA_F16 or SDPA_BF16.
+ *
+ * Supported head dims: (D, Dv) in {(64, 64), (128, 128)}.  q/k/v/o base pointers must be
+ * 16-byte aligned and their s/h/b strides multiples of 8 elements (tensor-memory-access
+ * descriptor rule); otherwise SDPA_ERR_UNSUPPORTED.  Sizes: B, Hq, Hkv, Sq, Sk >= 1.
+ */
+int sdpa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,
+             int Sk, int D, int Dv, const int64_t* strides, float scale, int causal, const void* mask,
+             const int64_t* mask_strides, void* workspace, size_t workspace_bytes, sdpa_dtype in_dtype,
+             sdpa_dtype out_dtype, void* stream);
+
+/*
+ * sdpa_fwd_fp8 -- the same prefill with FP8 e4m3 Q/K/V codes and per-tensor fp32 scales
+ * (Q = q_code * descale_q, likewise K and V; host floats).  Q K^T runs on e4m3 tensor
+ * cores with fp32 accumulation, the descales folded into the softmax scale; P and V
+ * meet in fp16 (every e4m3 value is exact in fp16) with fp32 accumulation; O is
+ * multiplied by descale_v in the epilogue.  (page "MlaMmaOp", struct summary: the
+ * MLA prefill path streams FP8 e4m3 K/V with D != Dv.)
+ *
+ * Supported head dims: (D, Dv) in {(128, 128), (192, 128)}.  q/k/v strides must be
+ * multiples of 16 elements.  out_dtype: SDPA_BF16 or SDPA_F16.  Other arguments as in
+ * sdpa_fwd.
+ */
+int sdpa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,
+                 int Sk, int D, int Dv, const int64_t* strides, float scale, int causal, const void* mask,
+                 const int64_t* mask_strides, void* workspace, size_t workspace_bytes, float descale_q,
+                 float descale_k, float descale_v, sdpa_dtype out_dtype, void* stream);
+
+/*
+ * sdpa_decode_workspace_size -- bytes of device scratch sdpa_decode needs for per-split
+ * partial results (unnormalised O, running max, running sum) of every (b, q-head, split).
+ */
+size_t sdpa_decode_workspace_size(int B, int Hq, int max_kv, int Dv);
+
+/*
+ * sdpa_decode -- two-phase split-KV decode: one query token per (b, query head) against
+ * the first kv_len[b] rows of a padded K/V cache.  Phase 1 gives every (b, kv head,
+ * split of keys) a partial (O, m, l); phase 2 merges the splits of a (b, q head) with a
+ * log-sum-exp combine.  Cache rows at or beyond kv_len[b] are never read.
+ * (page "Xe2 ESIMD Flash Attention", section "Assets": two-phase full-dense decode)
+ *
+ *   q       [B, Hq, D]                 dtype            o   [B, Hq, Dv]  dtype (written)
+ *   k_cache [B, max_kv, Hkv, D]        dtype            lse [B, Hq] fp32 contiguous or NULL
+ *   v_cache [B, max_kv, Hkv, Dv]       dtype
+ *   kv_len  [B] int32, DEVICE pointer, each in [0, max_kv]; kv_len[b] = 0 gives O = 0,
+ *           LSE = -inf.  Values outside [0, max_kv] are clamped into it on the device.
+ *   strides: NULL for the layouts above, else 10 element strides
+ *            {q_b, q_h,  k_b, k_s, k_h,  v_b, v_s, v_h,  o_b, o_h}
+ *   workspace: at least sdpa_decode_workspace_size(B, Hq, max_kv, Dv) bytes, 16-byte
+ *           aligned, device memory; its contents on entry do not matter.
+ *   dtype:  SDPA_F16 or SDPA_BF16.
+ *
+ * Supported: D = Dv = 128 and 1 <= Hq/Hkv <= 8; pointers 16-byte aligned; s/h/b strides
+ * multiples of 8 elements.
+ */
+int sdpa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_len, void* o, float* lse,
+                int B, int Hq, int Hkv, int max_kv, int D, int Dv, const int64_t* strides, float scale,
+                void* workspace, size_t workspace_bytes, sdpa_dtype dtype, void* stream);
+
+/*
+ * sdpa_check_device_status -- synchronizes `stream`, then reports and clears the device
+ * status word the kernels raise when a bounded wait inside them gives up (a pipeline
+ * stage that never arrived): SDPA_ERR_TIMEOUT in that case, SDPA_ERR_CUDA if the
+ * synchronization itself failed, else SDPA_OK.  The status word is per device and per
+ * process, shared by all streams.
+ */
+int sdpa_check_device_status(void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* sdpa_status_string(int status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int sdpa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDPA_GB300_H */
