@@ -1,0 +1,487 @@
+#!/usr/bin/env python3
+"""Throughput benchmark of the SDPA forward library on synthetic workloads.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--headline-only]
+
+One step of the headline workload is one fused prefill launch over the GQA causal
+batch (B=2, Hq=32, Hkv=8, Sq=Sk=4096, D=Dv=128, bf16); `value` is its throughput in
+TFLOP/s of algorithmic work (2 (D + Dv) per visible query/key pair), inputs resident in
+HBM, L2 flushed before every timed step.  The other workloads (tiny fp16 prefill,
+unaligned + additive mask, split-KV decode in GB/s, MLA FP8 prefill) are timed the same way
+and reported under "workloads".  For N > 1 (torchrun) every rank runs the same workload on
+its own GPU (replicas; no collective on the data path) and `value` sums the ranks' work over
+the slowest rank's time.
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same workload on the
+host cores (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s (prefill) & HBM GB/s (decode), % of GB300 roofline"
+HEADLINE = "gqa_causal_prefill_bf16_d128"
+L2_FLUSH_BYTES = 256 << 20
+FP8_PER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor ratio (4.5 / 2.25 PFLOP/s)
+
+
+# ----------------------------------------------------------------------------- work counts
+
+def visible_pairs(Sq: int, Sk: int, causal: bool) -> int:
+    """(i, j) pairs with key j visible to query i (top-left causal: j <= i)."""
+    if not causal:
+        return Sq * Sk
+    m = min(Sq, Sk)
+    return m * (m + 1) // 2 + max(0, Sq - Sk) * Sk
+
+
+def prefill_flops(w) -> float:
+    return 2.0 * (w.D + w.Dv) * w.B * w.Hq * visible_pairs(w.Sq, w.Sk, w.causal)
+
+
+def decode_bytes(w, kv_len) -> float:
+    esz = 2
+    kv = float(np.sum(np.asarray(kv_len, dtype=np.int64))) * w.Hkv * (w.D + w.Dv) * esz
+    return kv + w.B * w.Hq * (w.D + w.Dv) * esz
+
+
+# ----------------------------------------------------------------------------- environment
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def source_sha() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "flash_attention_forward_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu capture, if taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f).get(workload)
+    if not d or d.get("source_sha") != source_sha():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(float(r[2]) for r in rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit()) if rows else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- timing
+
+def time_steps(step, K: int, W: int, flush=None):
+    """W untimed steps, then K steps each bracketed by CUDA events on the launching stream
+    (an optional L2 flush runs before each step, outside the events).  Returns per-step ms."""
+    stream = torch.cuda.current_stream()
+    for _ in range(W):
+        if flush:
+            flush()
+        step(-1)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        if flush:
+            flush()
+        ev[i][0].record(stream)
+        step(i)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+class Flusher:
+    def __init__(self, dev):
+        self.buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def __call__(self):
+        self.buf.fill_(1)
+
+
+def prefill_setup(w, dev, rotation=0):
+    import flash_attention_forward_gb300 as fa
+
+    x = workloads.prefill_inputs(w, rotation)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    mask = x["mask"].to(dev) if x["mask"] is not None else None
+    out_dtype = torch.float16 if w.dtype == "f16" else torch.bfloat16
+    o = torch.empty((w.B, w.Sq, w.Hq, w.Dv), dtype=out_dtype, device=dev)
+    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+    ws = None
+    if mask is not None:
+        ws = torch.empty(fa.sdpa_fwd_workspace_size(w.B, w.Sq, w.Sk, True), dtype=torch.uint8, device=dev)
+    dq, dk, dv = x["descale"]
+
+    def step(_i=0):
+        if w.dtype == "e4m3":
+            fa.sdpa_fwd_fp8(q, k, v, dq, dk, dv, scale=w.scale, causal=w.causal, mask=mask, out=o, lse=lse,
+                            workspace=ws)
+        else:
+            fa.sdpa_fwd(q, k, v, scale=w.scale, causal=w.causal, mask=mask, out=o, lse=lse, workspace=ws)
+
+    return x, step
+
+
+def bench_prefill(w, K, W, dev, peaks, flusher):
+    _, step = prefill_setup(w, dev)
+    ms = time_steps(step, K, W, flusher)
+    flops = prefill_flops(w)
+    avg = sum(ms) / len(ms)
+    tflops = flops / (avg * 1e-3) / 1e12
+    launches = 1 + (1 if w.mask else 0)
+    bf16 = peaks["bf16_tflops"]
+    r = {"workload": w.name, "value": tflops, "unit": "TFLOP/s", "ms_per_step": avg, "flops_per_step": flops,
+         "launches_per_step": launches}
+    if w.dtype == "e4m3":
+        fp8 = bf16 * FP8_PER_BF16
+        qk = 2.0 * w.D * w.B * w.Hq * visible_pairs(w.Sq, w.Sk, w.causal)
+        pv = flops - qk
+        mixed = flops / (qk / fp8 + pv / bf16)
+        r["roofline"] = {"bound": "tensor", "achieved": tflops, "peak": fp8, "unit": "TFLOP/s", "frac": tflops / fp8,
+                         "peak_note": "FP8 = measured bf16 burst x 2 (nominal ratio); of measured",
+                         "mixed_ceiling": mixed, "frac_of_mixed_ceiling": tflops / mixed,
+                         "traffic": recorded_traffic(w.name)}
+    else:
+        r["roofline"] = {"bound": "tensor", "achieved": tflops, "peak": bf16, "unit": "TFLOP/s", "frac": tflops / bf16,
+                         "peak_note": "bf16 burst, of " + peaks["source"], "traffic": recorded_traffic(w.name)}
+    return r
+
+
+def bench_decode(w, K, W, dev, peaks):
+    import flash_attention_forward_gb300 as fa
+
+    sets = []
+    for r in range(4):  # rotating buffer sets, every one far larger than L2
+        x = workloads.decode_inputs(w, rotation=r, pad_value=0.0)
+        d = {n: x[n].to(dev) for n in ("q", "k", "v", "kv_len")}
+        d["bytes"] = decode_bytes(w, x["kv_len"].numpy())
+        sets.append(d)
+        del x
+    o = torch.empty((w.B, w.Hq, w.Dv), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+    ws = torch.empty(fa.sdpa_decode_workspace_size(w.B, w.Hq, w.Sk, w.Dv), dtype=torch.uint8, device=dev)
+
+    def step(i):
+        s = sets[i % 4] if i >= 0 else sets[0]
+        fa.sdpa_decode(s["q"], s["k"], s["v"], s["kv_len"], scale=w.scale, out=o, lse=lse, workspace=ws)
+
+    ms = time_steps(step, K, W)
+    by = [sets[i % 4]["bytes"] for i in range(K)]
+    gbs = [b / (t * 1e-3) / 1e9 for b, t in zip(by, ms)]
+    avg_ms = sum(ms) / K
+    value = sum(by) / (sum(ms) * 1e-3) / 1e9
+    hbm = peaks["hbm_gbs"]
+    return {"workload": w.name, "value": value, "unit": "GB/s", "ms_per_step": avg_ms, "bytes_per_step": sum(by) / K,
+            "launches_per_step": 2, "per_step_gbs_min": min(gbs),
+            "roofline": {"bound": "hbm", "achieved": value, "peak": hbm, "unit": "GB/s", "frac": value / hbm,
+                         "peak_note": "copy bandwidth, of " + peaks["source"], "traffic": recorded_traffic(w.name)}}
+
+
+def bench_e2e_prefill(w, K, dev):
+    """Same metric through the public API with host buffers: pinned host -> device copies of
+    the step's inputs, the call, device -> pinned host copies of O and LSE, all timed."""
+    import flash_attention_forward_gb300 as fa
+
+    x = workloads.prefill_inputs(w)
+    hq, hk, hv = (x[n].pin_memory() for n in ("q", "k", "v"))
+    dq, dk, dv = (torch.empty_like(t, device=dev) for t in (hq, hk, hv))
+    o = torch.empty((w.B, w.Sq, w.Hq, w.Dv), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def step(_i):
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        fa.sdpa_fwd(dq, dk, dv, scale=w.scale, causal=w.causal, out=o, lse=lse)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    ms = time_steps(step, K, 2)
+    avg = sum(ms) / len(ms)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    return {"value": prefill_flops(w) / (avg * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": avg,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample(w, target_s: float, seed: int = 0):
+    """Rows of the workload for a bounded oracle run: (inputs, rows, flops of those rows)."""
+    import oracle
+
+    x = workloads.prefill_inputs(w)
+    g = np.random.default_rng(seed)
+
+    def flops_of(rows):
+        vis = [min(i + 1, w.Sk) if w.causal else w.Sk for (_, _, i) in rows]
+        return 2.0 * (w.D + w.Dv) * float(sum(vis))
+
+    def pick(n):
+        b = g.integers(w.B, size=n)
+        h = g.integers(w.Hq, size=n)
+        i = g.integers(w.Sq, size=n)
+        return np.stack([b, h, i], axis=1).astype(np.int64)
+
+    probe = pick(256)
+    t0 = time.perf_counter()
+    oracle.sdpa_fwd(x["q"], x["k"], x["v"], x["mask"], scale=w.scale, causal=w.causal, rows=probe,
+                    descale=x["descale"])
+    dt = max(time.perf_counter() - t0, 1e-3)
+    n = int(max(256, min(w.B * w.Hq * w.Sq, 256 * target_s / dt)))
+    rows = pick(n)
+    return x, rows, flops_of(rows)
+
+
+def run_oracle(w, x, rows):
+    import oracle
+
+    t0 = time.perf_counter()
+    oracle.sdpa_fwd(x["q"], x["k"], x["v"], x["mask"], scale=w.scale, causal=w.causal, rows=rows,
+                    descale=x["descale"])
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, target_s=15.0):
+    import oracle
+
+    x, rows, flops = oracle_sample(w, target_s)
+    t = run_oracle(w, x, rows)
+    return {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"{len(rows)} random query rows (b, h, i) of {w.name}, fp64, {t:.1f} s on the host cores",
+            "seconds": t}
+
+
+# ----------------------------------------------------------------------------- main
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world <= 1:
+        return 0, 0, 1
+    import torch.distributed as dist
+
+    rank = int(os.environ["RANK"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    torch.cuda.set_device(local)
+    dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return rank, local, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def config_of(w):
+    c = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "D": w.D, "Dv": w.Dv,
+         "dtype": w.dtype, "causal": w.causal, "mask": w.mask}
+    return c
+
+
+def main_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    w = workloads.WORKLOADS[HEADLINE]
+    per_step_s = max(1.0, 150.0 / max(1, args.steps + args.warmup))
+    x, rows, flops = oracle_sample(w, per_step_s)
+    for _ in range(args.warmup):
+        run_oracle(w, x, rows)
+    ts = [run_oracle(w, x, rows) for _ in range(args.steps)]
+    total = sum(ts)
+    value = flops * len(ts) / total / 1e12
+    cfg = config_of(w)
+    cfg["l2"] = "n/a (host CPU)"
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total / len(ts) * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg, "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(), "kind": "oracle",
+                             "sample": f"each step: {len(rows)} random query rows of {w.name} in fp64"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank, local, world = dist_setup()
+    if args.impl == "reference":
+        main_reference(args, rank, world)
+        return
+
+    import flash_attention_forward_gb300 as fa
+
+    fa.library()  # fails loudly if the CUDA library was not built
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    flusher = Flusher(dev)
+    w = workloads.WORKLOADS[HEADLINE]
+
+    # ---- headline: timed region bracketed by barrier + synchronize, max over ranks
+    _, step = prefill_setup(w, dev)
+    for _ in range(args.warmup):
+        flusher()
+        step()
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    ms = time_steps(step, args.steps, 0, flusher)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if rank == 0 else None
+    ok_status = fa.sdpa_check_device_status()
+    total_ms = max_over_ranks(sum(ms), world)
+    flops = prefill_flops(w)
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    avg_kernel_ms = sum(ms) / len(ms)
+    achieved = flops / (avg_kernel_ms * 1e-3) / 1e12
+    bf16 = peaks["bf16_tflops"]
+
+    e2e = bench_e2e_prefill(w, min(args.steps, 20), dev)
+    e2e_ms = max_over_ranks(e2e["ms_per_step"], world)
+    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+
+    others = {}
+    if not args.headline_only and rank == 0:
+        k2 = min(args.steps, 100)
+        for name in ("tiny_prefill_f16_d64", "unaligned_mask_prefill_bf16_d128", "mla_fp8_causal_prefill_d192"):
+            others[name] = bench_prefill(workloads.WORKLOADS[name], k2, args.warmup, dev, peaks, flusher)
+            torch.cuda.empty_cache()
+        others["splitkv_decode_bf16_d128"] = bench_decode(workloads.WORKLOADS["splitkv_decode_bf16_d128"], k2,
+                                                          args.warmup, dev, peaks)
+        torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w)
+
+    if rank == 0:
+        cfg = config_of(w)
+        cfg["l2"] = "flushed before every timed step (256 MiB write, outside the events)"
+        cfg["parallelism"] = f"replicas x{world}"
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
+                         "frac": achieved / bf16, "traffic": recorded_traffic(w.name),
+                         "kernel": "prefill_kernel<bf16, D=128, Dv=128, causal>",
+                         "peak_note": "bf16 dense burst, of " + peaks["source"]},
+            "cpu_baseline": None if cpu is None else {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")},
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
+                    "d2h_bytes_per_step": e2e["d2h_bytes_per_step"]},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "device_status": fa.sdpa_status_string(ok_status),
+            "workloads": others,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -5,7 +5,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/sdpa.h"
+#include "sdpa.h"
 #include "internal.h"
 
 namespace sdpa {

@@ -27,6 +27,11 @@
 namespace sdpa {
 
 constexpr float kRescaleLog2 = 8.0f;
+// Register split (launch: 384 threads x 168): the load/MMA warpgroup gives registers to the
+// two softmax warpgroups.  128 * 88 + 256 * 200 = 62464 <= 384 * 168 = 64512.
+constexpr uint32_t kRegsControl = 88;
+constexpr uint32_t kRegsSoftmax = 200;
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kPrefillThreads * 168, "register split exceeds launch");
 constexpr float kLn2 = 0.6931471805599453f;
 
 template <int ELEM, int D, int DV>
@@ -53,7 +58,7 @@ struct PrefillCfg {
   static constexpr int OFF_BAR = OFF_VRAW + STAGES * VRAW_BYTES;
   // barriers, tmem base, abort flag; then 1 KB of slack so that the 1024-B alignment of the
   // dynamic shared window never pushes the last byte past the allocation
-  static constexpr int SMEM = OFF_BAR + 256 + 1024;
+  static constexpr int SMEM = OFF_BAR + 512 + 1024;
   static_assert(D % CH == 0 && DV % 64 == 0, "head dims must be multiples of 64");
   static_assert(Q_BYTES % 1024 == 0 && K_BYTES % 1024 == 0 && V_BYTES % 1024 == 0, "1 KB tile alignment");
 };
@@ -121,20 +126,22 @@ __device__ __forceinline__ uint4 e4m3x8_to_f16x8(uint2 in) {
   return out;
 }
 
-struct CtaWork {
+// One work tile: two consecutive 128-row query tiles of one (batch, query head).
+struct WorkTile {
   int b, h, kvh, q0;
   int n_t[kTilesPerCta];  // K/V blocks each query tile needs (0 = tile entirely past Sq)
-  int n_blocks;           // blocks streamed for the CTA = max over tiles
+  int n_blocks;           // blocks streamed for the work tile = max over its query tiles
 };
 
+// Work tiles in launch order.  Causal tiles at the bottom of the matrix see the most keys and
+// come first; within a row band the query heads of one KV group are adjacent, so the CTAs that
+// run them together share K/V through L2.
 template <bool CAUSAL>
-__device__ __forceinline__ CtaWork cta_work(const PrefillParams& p) {
-  CtaWork w;
+__device__ __forceinline__ WorkTile work_tile(const PrefillParams& p, int item) {
+  WorkTile w;
   const int bh_count = p.B * p.Hq;
-  const int lin = blockIdx.x;
-  const int bh = lin % bh_count;
-  const int rank = lin / bh_count;
-  // causal tiles at the bottom of the matrix see the most keys: launch them first
+  const int bh = item % bh_count;
+  const int rank = item / bh_count;
   const int ctile = CAUSAL ? (p.n_cta_tiles - 1 - rank) : rank;
   w.b = bh / p.Hq;
   w.h = bh % p.Hq;
@@ -158,6 +165,24 @@ __device__ __forceinline__ CtaWork cta_work(const PrefillParams& p) {
   return w;
 }
 
+// The k-th work tile of CTA c (snake order over the longest-first list: forward on even
+// rounds, backward on odd ones, which evens out the per-CTA totals of a causal schedule).
+__device__ __forceinline__ int nth_item(int k) {
+  const int G = gridDim.x;
+  return (k & 1) ? (k + 1) * G - 1 - (int)blockIdx.x : k * G + (int)blockIdx.x;
+}
+
+// Persistent kernel: CTA c processes work tiles nth_item(0), nth_item(1), ...  Every role walks
+// the same sequence; the mbarrier phases continue from one work tile to the next, counted per
+// role:
+//   q_full[t]  / q_empty[t] : Q tile t landed / its last QK MMA finished (Q buffer reusable)
+//   k_full[s] / k_empty[s]  : K block in ring stage s landed / its last QK MMA finished
+//   v_full[s] / v_empty[s]  : V block in ring stage s landed / its last P.V MMA finished
+//   v_ready[s]              : (e4m3) V of stage s converted to f16
+//   s_full[t]               : S_t = Q_t K^T finished
+//   p_full[t]               : P_t written to tensor memory (and O_t rescaled if needed)
+//   o_done[t]               : O_t += P_t V finished
+//   o_empty[t]              : the epilogue has read O_t (the next work tile may overwrite it)
 template <int ELEM, int D, int DV, bool CAUSAL, bool MASK>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -172,33 +197,40 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   uint8_t* sVraw = smem + C::OFF_VRAW;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars;                 // [2]
-  uint64_t* kv_full = q_full + 2;          // [ST]
-  uint64_t* kv_empty = kv_full + ST;       // [ST]
-  uint64_t* v_ready = kv_empty + ST;       // [ST] (e4m3: converted V ready)
+  uint64_t* q_empty = q_full + 2;          // [2]
+  uint64_t* k_full = q_empty + 2;          // [ST]
+  uint64_t* k_empty = k_full + ST;         // [ST]
+  uint64_t* v_full = k_empty + ST;         // [ST]
+  uint64_t* v_empty = v_full + ST;         // [ST]
+  uint64_t* v_ready = v_empty + ST;        // [ST]
   uint64_t* s_full = v_ready + ST;         // [2]
   uint64_t* p_full = s_full + 2;           // [2]
   uint64_t* o_done = p_full + 2;           // [2]
-  uint64_t* mma_done = o_done + 2;         // [1]
+  uint64_t* o_empty = o_done + 2;          // [2]
+  uint64_t* mma_done = o_empty + 2;        // [1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const CtaWork w = cta_work<CAUSAL>(p);
+  const int n_items = p.n_cta_tiles * p.B * p.Hq;
 
   if (tid == 0) {
-    mbar_init(&q_full[0], 1);
-    mbar_init(&q_full[1], 1);
-    for (int s = 0; s < ST; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
-      mbar_init(&v_ready[s], 64);
-    }
     for (int t = 0; t < 2; ++t) {
+      mbar_init(&q_full[t], 1);
+      mbar_init(&q_empty[t], 1);
       mbar_init(&s_full[t], 1);
       mbar_init(&p_full[t], 128);
       mbar_init(&o_done[t], 1);
+      mbar_init(&o_empty[t], 128);
+    }
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+      mbar_init(&v_ready[s], 64);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -214,104 +246,150 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
+    regs_dec<kRegsControl>();
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      for (int t = 0; t < kTilesPerCta; ++t) {
-        if (w.n_t[t] == 0) continue;
-        mbar_arrive_expect_tx(&q_full[t], C::Q_BYTES);
-        for (int c = 0; c < C::NCH_D; ++c)
-          tma_load_4d(sQ + t * C::Q_BYTES + c * kBlockQ * C::CHB, &tm_q, &q_full[t], c * C::CH, w.h,
-                      w.q0 + t * kBlockQ, w.b);
-      }
-      int issued = 0;
-      for (int j = 0; j < w.n_blocks; ++j) {
-        const int s = j % ST;
-        const int r = j / ST;
-        if (r > 0 && !mbar_wait(&kv_empty[s], (r - 1) & 1, abort_flag, p.status)) break;
-        mbar_arrive_expect_tx(&kv_full[s], C::K_BYTES + (ELEM == kE4M3 ? C::VRAW_BYTES : C::V_BYTES));
-        for (int c = 0; c < C::NCH_D; ++c)
-          tma_load_4d(sK + s * C::K_BYTES + c * kBlockK * C::CHB, &tm_k, &kv_full[s], c * C::CH, w.kvh,
-                      j * kBlockK, w.b);
-        if constexpr (ELEM == kE4M3) {
-          tma_load_4d(sVraw + s * C::VRAW_BYTES, &tm_v, &kv_full[s], 0, w.kvh, j * kBlockK, w.b);
-        } else {
-          for (int c = 0; c < C::NCH_V; ++c)
-            tma_load_4d(sV + s * C::V_BYTES + c * kBlockK * 128, &tm_v, &kv_full[s], c * 64, w.kvh, j * kBlockK,
-                        w.b);
+      int qn[2] = {0, 0};  // Q loads issued per tile slot
+      int g = 0;           // K/V blocks issued
+      bool ok = true;
+      for (int k = 0, item = nth_item(0); ok && item < n_items; item = nth_item(++k)) {
+        const WorkTile w = work_tile<CAUSAL>(p, item);
+        for (int t = 0; t < kTilesPerCta && ok; ++t) {
+          if (w.n_t[t] == 0) continue;
+          if (qn[t] > 0 && !mbar_wait(&q_empty[t], (qn[t] - 1) & 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&q_full[t], C::Q_BYTES);
+          for (int c = 0; c < C::NCH_D; ++c)
+            tma_load_4d(sQ + t * C::Q_BYTES + c * kBlockQ * C::CHB, &tm_q, &q_full[t], c * C::CH, w.h,
+                        w.q0 + t * kBlockQ, w.b);
+          ++qn[t];
         }
-        issued = j + 1;
+        for (int j = 0; ok && j < w.n_blocks; ++j, ++g) {
+          const int s = g % ST, r = g / ST;
+          if (r > 0 && !mbar_wait(&k_empty[s], (r - 1) & 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&k_full[s], C::K_BYTES);
+          for (int c = 0; c < C::NCH_D; ++c)
+            tma_load_4d(sK + s * C::K_BYTES + c * kBlockK * C::CHB, &tm_k, &k_full[s], c * C::CH, w.kvh,
+                        j * kBlockK, w.b);
+          if (r > 0 && !mbar_wait(&v_empty[s], (r - 1) & 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          if constexpr (ELEM == kE4M3) {
+            mbar_arrive_expect_tx(&v_full[s], C::VRAW_BYTES);
+            tma_load_4d(sVraw + s * C::VRAW_BYTES, &tm_v, &v_full[s], 0, w.kvh, j * kBlockK, w.b);
+          } else {
+            mbar_arrive_expect_tx(&v_full[s], C::V_BYTES);
+            for (int c = 0; c < C::NCH_V; ++c)
+              tma_load_4d(sV + s * C::V_BYTES + c * kBlockK * 128, &tm_v, &v_full[s], c * 64, w.kvh,
+                          j * kBlockK, w.b);
+          }
+        }
       }
-      if (*abort_flag) {
+      if (!ok) {
         // let every copy already in flight land before the CTA's shared memory goes away
         for (int t = 0; t < kTilesPerCta; ++t)
-          if (w.n_t[t] > 0) mbar_drain(&q_full[t], 0);
-        for (int j = max(0, issued - ST); j < issued; ++j) mbar_drain(&kv_full[j % ST], (j / ST) & 1);
+          if (qn[t] > 0) mbar_drain(&q_full[t], (qn[t] - 1) & 1);
+        for (int j = max(0, g - ST); j < g; ++j) {
+          mbar_drain(&k_full[j % ST], (j / ST) & 1);
+          mbar_drain(&v_full[j % ST], (j / ST) & 1);
+        }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (one thread)
+    regs_dec<kRegsControl>();
     if (lane == 0) {
       constexpr uint32_t idesc_qk =
           make_idesc(ElemTraits<ELEM>::qk_fmt, ElemTraits<ELEM>::qk_fmt, 0, 0, kBlockQ, kBlockK);
       constexpr uint32_t idesc_pv = make_idesc(ElemTraits<ELEM>::pv_fmt, ElemTraits<ELEM>::pv_fmt, 0, 1, kBlockQ, DV);
       const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
+      int qn[2] = {0, 0};   // work tiles seen per tile slot (q_full / q_empty / o_empty phases)
+      int pn[2] = {0, 0};   // P.V blocks issued per tile slot (p_full / o_done phases)
+      int g = 0;            // K/V blocks consumed
       bool ok = true;
-      for (int t = 0; t < kTilesPerCta && ok; ++t)
-        if (w.n_t[t] > 0) ok = mbar_wait(&q_full[t], 0, abort_flag, p.status);
-      for (int j = 0; ok && j <= w.n_blocks; ++j) {
-        const int s = j % ST, r = j / ST;
-        const int sp = (j + ST - 1) % ST, rp = (j - 1) / ST;  // stage / round of block j-1
-        bool k_ready = false;
-        if (ELEM == kE4M3 && j >= 1) {
-          if (!mbar_wait(&v_ready[sp], rp & 1, abort_flag, p.status)) break;
-        }
-        for (int t = 0; t < kTilesPerCta; ++t) {
-          const uint32_t tS = tmem_base + t * 128;
-          const uint32_t tO = tmem_base + 256 + t * 128;
-          // O_t += P_t(j-1) V(j-1), with P read from tensor memory
-          if (j >= 1 && j - 1 < w.n_t[t]) {
-            if (!mbar_wait(&p_full[t], (j - 1) & 1, abort_flag, p.status)) {
+      for (int k = 0, item = nth_item(0); ok && item < n_items; item = nth_item(++k)) {
+        const WorkTile w = work_tile<CAUSAL>(p, item);
+        for (int t = 0; t < kTilesPerCta && ok; ++t)
+          if (w.n_t[t] > 0) ok = mbar_wait(&q_full[t], qn[t] & 1, abort_flag, p.status);
+        for (int j = 0; ok && j <= w.n_blocks; ++j) {
+          const int gj = g + j;                                  // this block
+          const int s = gj % ST, r = gj / ST;
+          const int sp = (gj + ST - 1) % ST, rp = (gj - 1) / ST;  // block j-1
+          bool k_ready = false;
+          if (j >= 1) {
+            // V of block j-1: converted to f16 (e4m3) or landed (16-bit)
+            uint64_t* vb = (ELEM == kE4M3) ? &v_ready[sp] : &v_full[sp];
+            if (!mbar_wait(vb, rp & 1, abort_flag, p.status)) {
               ok = false;
               break;
             }
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < C::PV_STEPS; ++kk) {
-              const uint64_t bdesc =
-                  make_smem_desc(sVa + sp * C::V_BYTES + kk * 16 * 128, kBlockK * 128, 1024, kSwizzle128B);
-              mma_f16_ts(tO, tS + kk * 8, bdesc, idesc_pv, (j - 1 > 0 || kk > 0) ? 1u : 0u);
-            }
-            mma_commit(&o_done[t]);
           }
-          // block j-1 is no longer needed once the MMAs issued so far complete
-          if (t == kTilesPerCta - 1 && j >= 1) mma_commit(&kv_empty[sp]);
-          // S_t = Q_t K(j)^T
-          if (j < w.n_t[t]) {
-            if (!k_ready) {
-              if (!mbar_wait(&kv_full[s], r & 1, abort_flag, p.status)) {
+          for (int t = 0; t < kTilesPerCta; ++t) {
+            const uint32_t tS = tmem_base + t * 128;
+            const uint32_t tO = tmem_base + 256 + t * 128;
+            // O_t += P_t(j-1) V(j-1), with P read from tensor memory
+            if (j >= 1 && j - 1 < w.n_t[t]) {
+              // the first P.V of a work tile overwrites O_t: the previous epilogue must be done
+              if (j == 1 && qn[t] > 0 && !mbar_wait(&o_empty[t], (qn[t] - 1) & 1, abort_flag, p.status)) {
+                ok = false;
+                break;
+              }
+              if (!mbar_wait(&p_full[t], pn[t] & 1, abort_flag, p.status)) {
                 ok = false;
                 break;
               }
               tc_fence_after();
-              k_ready = true;
-            }
 #pragma unroll
-            for (int kk = 0; kk < C::QK_STEPS; ++kk) {
-              const int ch = kk / C::STEPS_PER_CH;
-              const uint32_t off = ch * kBlockQ * C::CHB + (kk % C::STEPS_PER_CH) * C::KSTEP_BYTES;
-              const uint64_t adesc = make_smem_desc(sQa + t * C::Q_BYTES + off, 16, 8 * C::CHB, C::SW);
-              const uint64_t bdesc = make_smem_desc(sKa + s * C::K_BYTES + off, 16, 8 * C::CHB, C::SW);
-              if constexpr (ELEM == kE4M3)
-                mma_f8_ss(tS, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
-              else
-                mma_f16_ss(tS, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+              for (int kk = 0; kk < C::PV_STEPS; ++kk) {
+                const uint64_t bdesc =
+                    make_smem_desc(sVa + sp * C::V_BYTES + kk * 16 * 128, kBlockK * 128, 1024, kSwizzle128B);
+                mma_f16_ts(tO, tS + kk * 8, bdesc, idesc_pv, (j - 1 > 0 || kk > 0) ? 1u : 0u);
+              }
+              mma_commit(&o_done[t]);
+              ++pn[t];
             }
-            mma_commit(&s_full[t]);
+            // V of block j-1 is no longer needed once the MMAs issued so far complete
+            if (t == kTilesPerCta - 1 && j >= 1) mma_commit(&v_empty[sp]);
+            // S_t = Q_t K(j)^T
+            if (j < w.n_t[t]) {
+              if (!k_ready) {
+                if (!mbar_wait(&k_full[s], r & 1, abort_flag, p.status)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                k_ready = true;
+              }
+#pragma unroll
+              for (int kk = 0; kk < C::QK_STEPS; ++kk) {
+                const int ch = kk / C::STEPS_PER_CH;
+                const uint32_t off = ch * kBlockQ * C::CHB + (kk % C::STEPS_PER_CH) * C::KSTEP_BYTES;
+                const uint64_t adesc = make_smem_desc(sQa + t * C::Q_BYTES + off, 16, 8 * C::CHB, C::SW);
+                const uint64_t bdesc = make_smem_desc(sKa + s * C::K_BYTES + off, 16, 8 * C::CHB, C::SW);
+                if constexpr (ELEM == kE4M3)
+                  mma_f8_ss(tS, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+                else
+                  mma_f16_ss(tS, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+              }
+              mma_commit(&s_full[t]);
+              if (j == w.n_t[t] - 1) mma_commit(&q_empty[t]);  // Q_t of this work tile fully used
+            }
           }
+          // K of block j is no longer needed once its QK MMAs complete
+          if (ok && j < w.n_blocks) mma_commit(&k_empty[s]);
         }
+        g += w.n_blocks;
+        for (int t = 0; t < kTilesPerCta; ++t)
+          if (w.n_t[t] > 0) ++qn[t];
       }
       // every MMA issued so far has finished before tensor memory is released
       mma_commit(mma_done);
@@ -319,199 +397,227 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     }
   } else if (warp < 4) {
     // ------------------------------------------------------------ e4m3 V -> f16 converter
+    regs_dec<kRegsControl>();
     if constexpr (ELEM == kE4M3) {
       const int ct = tid - 64;  // 0..63
-      for (int j = 0; j < w.n_blocks; ++j) {
-        const int s = j % ST, r = j / ST;
-        if (!mbar_wait(&kv_full[s], r & 1, abort_flag, p.status)) break;
-        const uint8_t* src = sVraw + s * C::VRAW_BYTES;
-        uint8_t* dst = sV + s * C::V_BYTES;
-        constexpr int UNITS = kBlockK * DV / 8;  // 8 values per unit
+      int g = 0;
+      bool ok = true;
+      for (int k = 0, item = nth_item(0); ok && item < n_items; item = nth_item(++k)) {
+        const WorkTile w = work_tile<CAUSAL>(p, item);
+        for (int j = 0; j < w.n_blocks; ++j, ++g) {
+          const int s = g % ST, r = g / ST;
+          if (!mbar_wait(&v_full[s], r & 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          const uint8_t* src = sVraw + s * C::VRAW_BYTES;
+          uint8_t* dst = sV + s * C::V_BYTES;
+          constexpr int UNITS = kBlockK * DV / 8;  // 8 values per unit
 #pragma unroll 4
-        for (int u = ct; u < UNITS; u += 64) {
-          const int row = u / (DV / 8), du = u % (DV / 8);
-          const int ch = du >> 3, uc = du & 7;
-          const uint2 raw = *reinterpret_cast<const uint2*>(src + row * DV + du * 8);
-          *reinterpret_cast<uint4*>(dst + ch * kBlockK * 128 + row * 128 + ((uc ^ (row & 7)) << 4)) =
-              e4m3x8_to_f16x8(raw);
+          for (int u = ct; u < UNITS; u += 64) {
+            const int row = u / (DV / 8), du = u % (DV / 8);
+            const int ch = du >> 3, uc = du & 7;
+            const uint2 raw = *reinterpret_cast<const uint2*>(src + row * DV + du * 8);
+            *reinterpret_cast<uint4*>(dst + ch * kBlockK * 128 + row * 128 + ((uc ^ (row & 7)) << 4)) =
+                e4m3x8_to_f16x8(raw);
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(&v_ready[s]);
         }
-        fence_proxy_async_smem();
-        mbar_arrive(&v_ready[s]);
       }
     }
   } else {
     // ------------------------------------------------------------ softmax warpgroups
-    const int t = (warp - 4) >> 2;           // query tile of this warpgroup
+    regs_inc<kRegsSoftmax>();
+    const int t = (warp - 4) >> 2;           // query tile slot of this warpgroup
     const int wq = warp & 3;                 // tensor-memory lane quarter
     const int row = wq * 32 + lane;          // row within the tile
-    const int qrow = w.q0 + t * kBlockQ + row;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem_base + lane_off + t * 128;
     const uint32_t tO = tmem_base + lane_off + 256 + t * 128;
-    const int n = w.n_t[t];
     const float scale2 = p.scale2;
-    float m_used = -INFINITY;
-    float l = 0.f;
+    int sn = 0;  // S blocks consumed (s_full / p_full / o_done phases)
     bool ok = true;
-    const bool row_valid = qrow < p.Sq;
-    const uint4* bits_row = nullptr;
-    const uint8_t* flags_row = nullptr;
-    if constexpr (MASK) {
-      const int qr = row_valid ? qrow : 0;
-      bits_row = p.mask_bits + (static_cast<int64_t>(w.b) * p.Sq + qr) * p.n_kblocks;
-      flags_row = p.mask_flags + (static_cast<int64_t>(w.b) * p.Sq + qr) * p.n_kblocks;
-    }
+    for (int k = 0, item = nth_item(0); ok && item < n_items; item = nth_item(++k)) {
+      const WorkTile w = work_tile<CAUSAL>(p, item);
+      const int n = w.n_t[t];
+      if (n == 0) continue;
+      const int qrow = w.q0 + t * kBlockQ + row;
+      const bool row_valid = qrow < p.Sq;
+      float m_used = -INFINITY;
+      float l = 0.f;
+      const uint4* bits_row = nullptr;
+      const uint8_t* flags_row = nullptr;
+      if constexpr (MASK) {
+        const int qr = row_valid ? qrow : 0;
+        bits_row = p.mask_bits + (static_cast<int64_t>(w.b) * p.Sq + qr) * p.n_kblocks;
+        flags_row = p.mask_flags + (static_cast<int64_t>(w.b) * p.Sq + qr) * p.n_kblocks;
+      }
 
-    for (int j = 0; j < n; ++j) {
-      uint4 mbits = make_uint4(0u, 0u, 0u, 0u);
-      uint32_t mflag = 0;
-      if constexpr (MASK) {
-        if (row_valid) {
-          mbits = __ldg(bits_row + j);
-          mflag = __ldg(flags_row + j);
-        }
-      }
-      if (!mbar_wait_warp(&s_full[t], j & 1, abort_flag, p.status)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float s[kBlockK];
-      {
-        uint32_t r0[32], r1[32], r2[32], r3[32];
-        tmem_ld32(tS + 0, r0);
-        tmem_ld32(tS + 32, r1);
-        tmem_ld32(tS + 64, r2);
-        tmem_ld32(tS + 96, r3);
-        tmem_ld_wait();
-        reg_fence(r0);
-        reg_fence(r1);
-        reg_fence(r2);
-        reg_fence(r3);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          s[c] = __uint_as_float(r0[c]);
-          s[32 + c] = __uint_as_float(r1[c]);
-          s[64 + c] = __uint_as_float(r2[c]);
-          s[96 + c] = __uint_as_float(r3[c]);
-        }
-      }
-      // the causal diagonal and the ragged last block: hide keys past the row / past Sk
-      const int k0 = j * kBlockK;
-      const bool edge = (CAUSAL && (k0 + kBlockK - 1 > w.q0 + t * kBlockQ)) || (k0 + kBlockK > p.Sk);
-      if (edge) {
-        const int lim = (CAUSAL ? min(p.Sk, qrow + 1) : p.Sk) - k0;
-#pragma unroll
-        for (int c = 0; c < kBlockK; ++c)
-          if (c >= lim) s[c] = -INFINITY;
-      }
-      if constexpr (MASK) {
-        if (mflag) {
-          // block row with finite non-zero mask values: add them (rare path)
-          const uint16_t* mrow = p.mask + static_cast<int64_t>(w.b) * p.mask_b + static_cast<int64_t>(qrow) * p.mask_i;
-#pragma unroll
-          for (int c = 0; c < kBlockK; ++c) {
-            if (k0 + c < p.Sk) {
-              const float mv = __half2float(__ushort_as_half(__ldg(mrow + k0 + c)));
-              s[c] += mv * p.inv_scale;
-            }
+      for (int j = 0; j < n; ++j, ++sn) {
+        uint4 mbits = make_uint4(0u, 0u, 0u, 0u);
+        uint32_t mflag = 0;
+        if constexpr (MASK) {
+          if (row_valid) {
+            mbits = __ldg(bits_row + j);
+            mflag = __ldg(flags_row + j);
           }
         }
-        __syncwarp();
-        const uint32_t mw[4] = {mbits.x, mbits.y, mbits.z, mbits.w};
-#pragma unroll
-        for (int c = 0; c < kBlockK; ++c)
-          if ((mw[c >> 5] >> (c & 31)) & 1u) s[c] = -INFINITY;
-      }
-      // block row max (scale2 > 0, so the max of s orders like the max of scale2 * s)
-      float mx[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = s[i];
-#pragma unroll
-      for (int c = 8; c < kBlockK; c += 8)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], s[c + i]);
-      const float mb = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      const float m_cand = fmaxf(m_used, mb * scale2);
-      const bool need = m_cand > m_used + kRescaleLog2;
-      const bool rescale = __any_sync(0xffffffffu, need);
-      float alpha = 1.f;
-      if (rescale) {
-        alpha = (m_cand == -INFINITY) ? 1.f : ex2(m_used - m_cand);
-        l *= alpha;
-        m_used = m_cand;
-      }
-      // P = exp2(scale2 * s - m), rounded to 16 bits; l sums the rounded values
-      const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-      {
-        uint32_t pk[32];
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-#pragma unroll
-          for (int w2 = 0; w2 < 32; ++w2) {
-            const int c = half * 64 + 2 * w2;
-            const float p0 = ex2(fmaf(s[c], scale2, neg_m));
-            const float p1 = ex2(fmaf(s[c + 1], scale2, neg_m));
-            pk[w2] = pack_p<ELEM>(p0, p1);
-            ls[w2 & 3] += p_lo<ELEM>(pk[w2]) + p_hi<ELEM>(pk[w2]);
-          }
-          tmem_st32(tS + half * 32, pk);
-        }
-      }
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      if (rescale && j > 0) {
-        // O holds P.V of blocks < j at the old max: wait for that MMA, then scale it
-        if (!mbar_wait_warp(&o_done[t], (j - 1) & 1, abort_flag, p.status)) {
+        if (!mbar_wait_warp(&s_full[t], sn & 1, abort_flag, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < DV / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
+        float s[kBlockK];
+        {
+          uint32_t r0[32], r1[32], r2[32], r3[32];
+          tmem_ld32(tS + 0, r0);
+          tmem_ld32(tS + 32, r1);
+          tmem_ld32(tS + 64, r2);
+          tmem_ld32(tS + 96, r3);
           tmem_ld_wait();
-          reg_fence(o);
+          reg_fence(r0);
+          reg_fence(r1);
+          reg_fence(r2);
+          reg_fence(r3);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(tO + c * 32, o);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&p_full[t]);
-    }
-
-    // ------------------------------------------------------------ epilogue: O / l, LSE
-    const bool go = __all_sync(0xffffffffu, ok && n > 0 && !*abort_flag);
-    if (go) {
-      if (mbar_wait_warp(&o_done[t], (n - 1) & 1, abort_flag, p.status)) {
-        tc_fence_after();
-        const float inv = (l > 0.f) ? p.out_scale / l : 0.f;
-        uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
-                        2 * (static_cast<int64_t>(w.b) * p.o_b + static_cast<int64_t>(qrow) * p.o_s +
-                             static_cast<int64_t>(w.h) * p.o_h);
-#pragma unroll 1
-        for (int c = 0; c < DV / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
-          tmem_ld_wait();
-          reg_fence(o);
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = pack_out<ELEM>(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
-          if (row_valid) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c * 64);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          for (int c = 0; c < 32; ++c) {
+            s[c] = __uint_as_float(r0[c]);
+            s[32 + c] = __uint_as_float(r1[c]);
+            s[64 + c] = __uint_as_float(r2[c]);
+            s[96 + c] = __uint_as_float(r3[c]);
           }
         }
-        if (p.lse != nullptr && row_valid)
-          p.lse[(static_cast<int64_t>(w.b) * p.Hq + w.h) * p.Sq + qrow] =
-              (l > 0.f) ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+        // the causal diagonal and the ragged last block: hide keys past the row / past Sk
+        const int k0 = j * kBlockK;
+        const bool edge = (CAUSAL && (k0 + kBlockK - 1 > w.q0 + t * kBlockQ)) || (k0 + kBlockK > p.Sk);
+        if (edge) {
+          const int lim = (CAUSAL ? min(p.Sk, qrow + 1) : p.Sk) - k0;
+#pragma unroll
+          for (int c = 0; c < kBlockK; ++c)
+            if (c >= lim) s[c] = -INFINITY;
+        }
+        if constexpr (MASK) {
+          if (mflag) {
+            // block row with finite non-zero mask values: add them (rare path)
+            const uint16_t* mrow =
+                p.mask + static_cast<int64_t>(w.b) * p.mask_b + static_cast<int64_t>(qrow) * p.mask_i;
+#pragma unroll
+            for (int c = 0; c < kBlockK; ++c) {
+              if (k0 + c < p.Sk) {
+                const float mv = __half2float(__ushort_as_half(__ldg(mrow + k0 + c)));
+                s[c] += mv * p.inv_scale;
+              }
+            }
+          }
+          __syncwarp();
+          const uint32_t mw[4] = {mbits.x, mbits.y, mbits.z, mbits.w};
+#pragma unroll
+          for (int c = 0; c < kBlockK; ++c)
+            if ((mw[c >> 5] >> (c & 31)) & 1u) s[c] = -INFINITY;
+        }
+        // block row max (scale2 > 0, so the max of s orders like the max of scale2 * s)
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[i], s[8 + i]);
+#pragma unroll
+        for (int gi = 1; gi < kBlockK / 16; ++gi)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[16 * gi + i], s[16 * gi + 8 + i]);
+        const float mb = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+        const float m_cand = fmaxf(m_used, mb * scale2);
+        const bool need = m_cand > m_used + kRescaleLog2;
+        const bool rescale = __any_sync(0xffffffffu, need);
+        float alpha = 1.f;
+        if (rescale) {
+          alpha = (m_cand == -INFINITY) ? 1.f : ex2(m_used - m_cand);
+          l *= alpha;
+          m_used = m_cand;
+        }
+        // P = exp2(scale2 * s - m), rounded to 16 bits; l sums the rounded values
+        const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+          uint32_t pk[32];
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+#pragma unroll
+            for (int w2 = 0; w2 < 32; ++w2) {
+              const int c = half * 64 + 2 * w2;
+              float x0, x1;
+              ffma2_scalar(x0, x1, s[c], s[c + 1], scale2, neg_m);
+              pk[w2] = pack_p<ELEM>(ex2(x0), ex2(x1));
+              if (w2 & 1)
+                fadd2(ls[2], ls[3], p_lo<ELEM>(pk[w2]), p_hi<ELEM>(pk[w2]));
+              else
+                fadd2(ls[0], ls[1], p_lo<ELEM>(pk[w2]), p_hi<ELEM>(pk[w2]));
+            }
+            tmem_st32(tS + half * 32, pk);
+          }
+        }
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        if (rescale && j > 0) {
+          // O holds P.V of blocks < j at the old max: wait for that MMA, then scale it
+          if (!mbar_wait_warp(&o_done[t], (sn - 1) & 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < DV / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_ld_wait();
+            reg_fence(o);
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              float a = __uint_as_float(o[i]), b = __uint_as_float(o[i + 1]);
+              fmul2_scalar(a, b, alpha);
+              o[i] = __float_as_uint(a);
+              o[i + 1] = __float_as_uint(b);
+            }
+            tmem_st32(tO + c * 32, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&p_full[t]);
       }
+      if (!ok) break;
+
+      // ---------------------------------------------------------- epilogue: O / l, LSE
+      if (!mbar_wait_warp(&o_done[t], (sn - 1) & 1, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float inv = (l > 0.f) ? p.out_scale / l : 0.f;
+      uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
+                      2 * (static_cast<int64_t>(w.b) * p.o_b + static_cast<int64_t>(qrow) * p.o_s +
+                           static_cast<int64_t>(w.h) * p.o_h);
+#pragma unroll 1
+      for (int c = 0; c < DV / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + c * 32, o);
+        tmem_ld_wait();
+        reg_fence(o);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_out<ELEM>(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+        if (row_valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 64);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+        __syncwarp();
+      }
+      // O_t has been read: the next work tile's first P.V may overwrite it
+      tc_fence_before();
+      mbar_arrive(&o_empty[t]);
+      if (p.lse != nullptr && row_valid)
+        p.lse[(static_cast<int64_t>(w.b) * p.Hq + w.h) * p.Sq + qrow] =
+            (l > 0.f) ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
     }
   }
 

@@ -13,8 +13,13 @@ cudaError_t launch_prefill_instance(const CUtensorMap& tq, const CUtensorMap& tk
   // the shared-memory opt-in is per device; setting it again is harmless
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  const long long grid = (long long)p.n_cta_tiles * p.B * p.Hq;
-  kern<<<(unsigned)grid, kPrefillThreads, C::SMEM, st>>>(tq, tk, tv, p);
+  // persistent: one CTA per SM (shared memory admits no second one), looping over work tiles
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const long long items = (long long)p.n_cta_tiles * p.B * p.Hq;
+  const unsigned grid = (unsigned)(items < sms ? items : sms);
+  kern<<<grid, kPrefillThreads, C::SMEM, st>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
