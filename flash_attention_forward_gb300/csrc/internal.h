@@ -17,6 +17,7 @@ constexpr int kBlockQ = 128;           // query rows per tile (one TMEM lane eac
 constexpr int kTilesPerCta = 2;        // two query tiles per CTA share every K/V block
 constexpr int kCtaRows = kBlockQ * kTilesPerCta;
 constexpr int kBlockK = 128;           // keys per K/V block
+static_assert(kBlockQ == kBlockK, "Q and K tiles share the descriptor chunk stride");
 constexpr int kPrefillThreads = 384;   // 12 warps: load, MMA, 2 helpers, 2 x 4 softmax
 
 enum ElemKind : int { kF16 = 0, kBF16 = 1, kE4M3 = 2 };

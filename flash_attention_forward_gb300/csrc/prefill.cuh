@@ -28,9 +28,9 @@ namespace sdpa {
 
 constexpr float kRescaleLog2 = 8.0f;
 // Register split (launch: 384 threads x 168): the load/MMA warpgroup gives registers to the
-// two softmax warpgroups.  128 * 88 + 256 * 200 = 62464 <= 384 * 168 = 64512.
-constexpr uint32_t kRegsControl = 88;
-constexpr uint32_t kRegsSoftmax = 200;
+// two softmax warpgroups.  128 * 104 + 256 * 192 = 62464 <= 384 * 168 = 64512.
+constexpr uint32_t kRegsControl = 80;
+constexpr uint32_t kRegsSoftmax = 208;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kPrefillThreads * 168, "register split exceeds launch");
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -311,7 +311,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       constexpr uint32_t idesc_qk =
           make_idesc(ElemTraits<ELEM>::qk_fmt, ElemTraits<ELEM>::qk_fmt, 0, 0, kBlockQ, kBlockK);
       constexpr uint32_t idesc_pv = make_idesc(ElemTraits<ELEM>::pv_fmt, ElemTraits<ELEM>::pv_fmt, 0, 1, kBlockQ, DV);
-      const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
+      // Descriptors are built once; a k-step or stage only moves the start address, whose
+      // field holds (address >> 4) in the low 14 bits, so an add of (offset >> 4) is exact
+      // for shared addresses below 256 KB.
+      const uint64_t dq0 = make_smem_desc(smem_u32(sQ), 16, 8 * C::CHB, C::SW);
+      const uint64_t dk0 = make_smem_desc(smem_u32(sK), 16, 8 * C::CHB, C::SW);
+      const uint64_t dv0 = make_smem_desc(smem_u32(sV), kBlockK * 128, 1024, kSwizzle128B);
       int qn[2] = {0, 0};   // work tiles seen per tile slot (q_full / q_empty / o_empty phases)
       int pn[2] = {0, 0};   // P.V blocks issued per tile slot (p_full / o_done phases)
       int g = 0;            // K/V blocks consumed
@@ -348,12 +353,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 break;
               }
               tc_fence_after();
+              const uint64_t dv = dv0 + (uint64_t)((sp * C::V_BYTES) >> 4);
+              const uint32_t acc0 = (j - 1 > 0) ? 1u : 0u;
 #pragma unroll
-              for (int kk = 0; kk < C::PV_STEPS; ++kk) {
-                const uint64_t bdesc =
-                    make_smem_desc(sVa + sp * C::V_BYTES + kk * 16 * 128, kBlockK * 128, 1024, kSwizzle128B);
-                mma_f16_ts(tO, tS + kk * 8, bdesc, idesc_pv, (j - 1 > 0 || kk > 0) ? 1u : 0u);
-              }
+              for (int kk = 0; kk < C::PV_STEPS; ++kk)
+                mma_f16_ts(tO, tS + kk * 8, dv + (uint64_t)((kk * 16 * 128) >> 4), idesc_pv, kk > 0 ? 1u : acc0);
               mma_commit(&o_done[t]);
               ++pn[t];
             }
@@ -369,16 +373,17 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 tc_fence_after();
                 k_ready = true;
               }
+              const uint64_t dq = dq0 + (uint64_t)((t * C::Q_BYTES) >> 4);
+              const uint64_t dk = dk0 + (uint64_t)((s * C::K_BYTES) >> 4);
 #pragma unroll
               for (int kk = 0; kk < C::QK_STEPS; ++kk) {
-                const int ch = kk / C::STEPS_PER_CH;
-                const uint32_t off = ch * kBlockQ * C::CHB + (kk % C::STEPS_PER_CH) * C::KSTEP_BYTES;
-                const uint64_t adesc = make_smem_desc(sQa + t * C::Q_BYTES + off, 16, 8 * C::CHB, C::SW);
-                const uint64_t bdesc = make_smem_desc(sKa + s * C::K_BYTES + off, 16, 8 * C::CHB, C::SW);
+                constexpr int kCh = kBlockQ * C::CHB;  // bytes per 64-element chunk (Q and K tiles alike)
+                const uint64_t off =
+                    (uint64_t)(((kk / C::STEPS_PER_CH) * kCh + (kk % C::STEPS_PER_CH) * C::KSTEP_BYTES) >> 4);
                 if constexpr (ELEM == kE4M3)
-                  mma_f8_ss(tS, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+                  mma_f8_ss(tS, dq + off, dk + off, idesc_qk, kk > 0 ? 1u : 0u);
                 else
-                  mma_f16_ss(tS, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+                  mma_f16_ss(tS, dq + off, dk + off, idesc_qk, kk > 0 ? 1u : 0u);
               }
               mma_commit(&s_full[t]);
               if (j == w.n_t[t] - 1) mma_commit(&q_empty[t]);  // Q_t of this work tile fully used
