@@ -210,3 +210,31 @@ def sdpa_decode(q, k_cache, v_cache, kv_len, *, scale: float | None = None, out=
 def sdpa_check_device_status(stream=None) -> int:
     """Synchronizes the stream and returns (and clears) the device status (SDPA_OK if clean)."""
     return int(_load().sdpa_check_device_status(_stream_ptr(stream)))
+
+
+def sdpa_decode_noalloc(q, k_cache, v_cache, kv_len, *, scale: float | None = None, out=None, lse=None,
+                        return_lse: bool = True, stream=None):
+    """sdpa_decode without a workspace: the per-split partials go to a fixed 32 MiB array inside
+    the library, for callers that cannot allocate device memory (e.g. under CUDA graph capture).
+
+    Such callers pass ``out`` (and ``lse``) themselves; this wrapper only allocates them when they
+    are omitted.  The first call on a device resolves the array's address and should precede any
+    stream capture; calls that overlap on the GPU share the array and race."""
+    lib = _load()
+    fn = lib.sdpa_decode_noalloc
+    p, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    fn.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, p, f, i, p]
+    fn.restype = i
+    B, Hq, D = q.shape
+    _, max_kv, Hkv, _ = k_cache.shape
+    Dv = v_cache.shape[-1]
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty((B, Hq, Dv), dtype=q.dtype, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    strides = _i64([*q.stride()[:2], *k_cache.stride()[:3], *v_cache.stride()[:3], *out.stride()[:2]])
+    rc = fn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_len), _ptr(out), _ptr(lse), B, Hq, Hkv, max_kv, D, Dv,
+            strides, scale, _DT[q.dtype], _stream_ptr(stream))
+    _check("sdpa_decode_noalloc", rc)
+    return out, lse

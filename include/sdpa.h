@@ -140,6 +140,27 @@ int sdpa_decode(const void* q, const void* k_cache, const void* v_cache, const i
                 void* workspace, size_t workspace_bytes, sdpa_dtype dtype, void* stream);
 
 /*
+ * sdpa_decode_noalloc -- sdpa_decode for callers that cannot allocate device memory: code
+ * that runs while a CUDA graph is being captured, allocator-free runtimes, and hosts that
+ * hand out device memory only through their own pool.  The pages this library follows have
+ * no counterpart for it.
+ *
+ * Arguments and results are those of sdpa_decode without the workspace: the per-split
+ * partials go to a fixed 32 MiB array in the library's own device memory, which every GPU
+ * that loads the library holds until the process exits.  A call that would need more
+ * (B * Hq * ceil(max_kv / 1024) * (Dv + 2) * 4 bytes > 32 MiB) returns SDPA_ERR_UNSUPPORTED
+ * and launches nothing.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before any stream
+ * capture.  All calls on a device share the array and it keeps the last call's contents
+ * (the decode rewrites every partial it reads, so nothing needs clearing); calls whose
+ * kernels overlap on the GPU race on it.  No cudaMalloc, cudaFree or allocating library
+ * routine is called.
+ */
+int sdpa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_len, void* o,
+                        float* lse, int B, int Hq, int Hkv, int max_kv, int D, int Dv, const int64_t* strides,
+                        float scale, sdpa_dtype dtype, void* stream);
+
+/*
  * sdpa_check_device_status -- synchronizes `stream`, then reports and clears the device
  * status word the kernels raise when a bounded wait inside them gives up (a pipeline
  * stage that never arrived): SDPA_ERR_TIMEOUT in that case, SDPA_ERR_CUDA if the
