@@ -28,9 +28,9 @@ namespace sdpa {
 
 constexpr float kRescaleLog2 = 8.0f;
 // Register split (launch: 384 threads x 168): the load/MMA warpgroup gives registers to the
-// two softmax warpgroups.  128 * 104 + 256 * 192 = 62464 <= 384 * 168 = 64512.
-constexpr uint32_t kRegsControl = 80;
-constexpr uint32_t kRegsSoftmax = 208;
+// two softmax warpgroups.  128 * 96 + 256 * 200 = 63488 <= 384 * 168 = 64512.
+constexpr uint32_t kRegsControl = 96;
+constexpr uint32_t kRegsSoftmax = 200;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kPrefillThreads * 168, "register split exceeds launch");
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -176,12 +176,19 @@ __device__ __forceinline__ int nth_item(int k) {
 // the same sequence; the mbarrier phases continue from one work tile to the next, counted per
 // role:
 //   q_full[t]  / q_empty[t] : Q tile t landed / its last QK MMA finished (Q buffer reusable)
-//   k_full[s] / k_empty[s]  : K block in ring stage s landed / its last QK MMA finished
-//   v_full[s] / v_empty[s]  : V block in ring stage s landed / its last P.V MMA finished
-//   v_ready[s]              : (e4m3) V of stage s converted to f16
+//   16-bit inputs, one ring whose step j holds what MMA step j reads:
+//   in_full[s]              : K(j) (j < n_blocks) and V(j-1) (j >= 1) landed in stage s
+//   released[s]             : every MMA that read stage s has finished (one commit per step)
+//   e4m3 inputs, where V(j) must also be converted to f16 before P V(j), K(j) and V(j) load
+//   together one step ahead of their P.V:
+//   in_full[s] / released[s]: K(j) landed / its QK MMAs finished
+//   v_full[s] / v_free[s]   : raw V(j) landed / P V(j) finished (raw and converted V free)
+//   v_ready[s]              : V(j) converted to f16
 //   s_full[t]               : S_t = Q_t K^T finished
 //   p_full[t]               : P_t written to tensor memory (and O_t rescaled if needed)
-//   o_done[t]               : O_t += P_t V finished
+//   o_full[t]               : the last P_t V of the work tile finished (epilogue may read O_t)
+// A rescale of O_t needs no barrier of its own: the commit behind s_full[t] for block j also
+// covers the P_t V of block j-1, which the same thread issued earlier.
 //   o_empty[t]              : the epilogue has read O_t (the next work tile may overwrite it)
 template <int ELEM, int D, int DV, bool CAUSAL, bool MASK>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
@@ -198,15 +205,15 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars;                 // [2]
   uint64_t* q_empty = q_full + 2;          // [2]
-  uint64_t* k_full = q_empty + 2;          // [ST]
-  uint64_t* k_empty = k_full + ST;         // [ST]
-  uint64_t* v_full = k_empty + ST;         // [ST]
-  uint64_t* v_empty = v_full + ST;         // [ST]
-  uint64_t* v_ready = v_empty + ST;        // [ST]
+  uint64_t* in_full = q_empty + 2;         // [ST] 16-bit: K(j) + V(j-1); e4m3: K(j)
+  uint64_t* released = in_full + ST;       // [ST] 16-bit: stage free; e4m3: K stage free
+  uint64_t* v_full = released + ST;        // [ST] e4m3: raw V(j) landed
+  uint64_t* v_free = v_full + ST;          // [ST] e4m3: V stage (raw and converted) free
+  uint64_t* v_ready = v_free + ST;         // [ST] e4m3: V(j) converted to f16
   uint64_t* s_full = v_ready + ST;         // [2]
   uint64_t* p_full = s_full + 2;           // [2]
-  uint64_t* o_done = p_full + 2;           // [2]
-  uint64_t* o_empty = o_done + 2;          // [2]
+  uint64_t* o_full = p_full + 2;           // [2]
+  uint64_t* o_empty = o_full + 2;          // [2]
   uint64_t* mma_done = o_empty + 2;        // [1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -222,14 +229,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       mbar_init(&q_empty[t], 1);
       mbar_init(&s_full[t], 1);
       mbar_init(&p_full[t], 128);
-      mbar_init(&o_done[t], 1);
+      mbar_init(&o_full[t], 1);
       mbar_init(&o_empty[t], 128);
     }
     for (int s = 0; s < ST; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
+      mbar_init(&in_full[s], 1);
+      mbar_init(&released[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
+      mbar_init(&v_free[s], 1);
       mbar_init(&v_ready[s], 64);
     }
     mbar_init(mma_done, 1);
@@ -253,7 +260,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       int qn[2] = {0, 0};  // Q loads issued per tile slot
-      int g = 0;           // K/V blocks issued
+      int g = 0;           // ring steps issued
       bool ok = true;
       for (int k = 0, item = nth_item(0); ok && item < n_items; item = nth_item(++k)) {
         const WorkTile w = work_tile<CAUSAL>(p, item);
@@ -269,28 +276,50 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                         w.q0 + t * kBlockQ, w.b);
           ++qn[t];
         }
-        for (int j = 0; ok && j < w.n_blocks; ++j, ++g) {
-          const int s = g % ST, r = g / ST;
-          if (r > 0 && !mbar_wait(&k_empty[s], (r - 1) & 1, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&k_full[s], C::K_BYTES);
-          for (int c = 0; c < C::NCH_D; ++c)
-            tma_load_4d(sK + s * C::K_BYTES + c * kBlockK * C::CHB, &tm_k, &k_full[s], c * C::CH, w.kvh,
-                        j * kBlockK, w.b);
-          if (r > 0 && !mbar_wait(&v_empty[s], (r - 1) & 1, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          if constexpr (ELEM == kE4M3) {
+        if constexpr (ELEM == kE4M3) {
+          // step j brings K(j) and raw V(j)
+          for (int j = 0; ok && j < w.n_blocks; ++j, ++g) {
+            const int s = g % ST, r = g / ST;
+            if (r > 0 && !mbar_wait(&released[s], (r - 1) & 1, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&in_full[s], C::K_BYTES);
+            for (int c = 0; c < C::NCH_D; ++c)
+              tma_load_4d(sK + s * C::K_BYTES + c * kBlockK * C::CHB, &tm_k, &in_full[s], c * C::CH, w.kvh,
+                          j * kBlockK, w.b);
+            if (r > 0 && !mbar_wait(&v_free[s], (r - 1) & 1, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
             mbar_arrive_expect_tx(&v_full[s], C::VRAW_BYTES);
             tma_load_4d(sVraw + s * C::VRAW_BYTES, &tm_v, &v_full[s], 0, w.kvh, j * kBlockK, w.b);
-          } else {
-            mbar_arrive_expect_tx(&v_full[s], C::V_BYTES);
-            for (int c = 0; c < C::NCH_V; ++c)
-              tma_load_4d(sV + s * C::V_BYTES + c * kBlockK * 128, &tm_v, &v_full[s], c * 64, w.kvh,
+          }
+          continue;
+        }
+        // step j of the work tile brings K(j) and V(j-1)
+        for (int j = 0; ok && j <= w.n_blocks; ++j, ++g) {
+          const int s = g % ST, r = g / ST;
+          const bool has_k = j < w.n_blocks, has_v = j >= 1;
+          if (r > 0 && !mbar_wait(&released[s], (r - 1) & 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          constexpr uint32_t v_bytes = (ELEM == kE4M3) ? C::VRAW_BYTES : C::V_BYTES;
+          mbar_arrive_expect_tx(&in_full[s], (has_k ? C::K_BYTES : 0) + (has_v ? v_bytes : 0));
+          if (has_k) {
+            for (int c = 0; c < C::NCH_D; ++c)
+              tma_load_4d(sK + s * C::K_BYTES + c * kBlockK * C::CHB, &tm_k, &in_full[s], c * C::CH, w.kvh,
                           j * kBlockK, w.b);
+          }
+          if (has_v) {
+            if constexpr (ELEM == kE4M3) {
+              tma_load_4d(sVraw + s * C::VRAW_BYTES, &tm_v, &in_full[s], 0, w.kvh, (j - 1) * kBlockK, w.b);
+            } else {
+              for (int c = 0; c < C::NCH_V; ++c)
+                tma_load_4d(sV + s * C::V_BYTES + c * kBlockK * 128, &tm_v, &in_full[s], c * 64, w.kvh,
+                            (j - 1) * kBlockK, w.b);
+            }
           }
         }
       }
@@ -299,8 +328,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         for (int t = 0; t < kTilesPerCta; ++t)
           if (qn[t] > 0) mbar_drain(&q_full[t], (qn[t] - 1) & 1);
         for (int j = max(0, g - ST); j < g; ++j) {
-          mbar_drain(&k_full[j % ST], (j / ST) & 1);
-          mbar_drain(&v_full[j % ST], (j / ST) & 1);
+          mbar_drain(&in_full[j % ST], (j / ST) & 1);
+          if (ELEM == kE4M3) mbar_drain(&v_full[j % ST], (j / ST) & 1);
         }
       }
     }
@@ -317,27 +346,34 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       const uint64_t dq0 = make_smem_desc(smem_u32(sQ), 16, 8 * C::CHB, C::SW);
       const uint64_t dk0 = make_smem_desc(smem_u32(sK), 16, 8 * C::CHB, C::SW);
       const uint64_t dv0 = make_smem_desc(smem_u32(sV), kBlockK * 128, 1024, kSwizzle128B);
-      int qn[2] = {0, 0};   // work tiles seen per tile slot (q_full / q_empty / o_empty phases)
-      int pn[2] = {0, 0};   // P.V blocks issued per tile slot (p_full / o_done phases)
-      int g = 0;            // K/V blocks consumed
+      int qn[2] = {0, 0};   // work tiles seen per tile slot (q_full / q_empty / o_full / o_empty phases)
+      int pn[2] = {0, 0};   // P.V blocks issued per tile slot (p_full phases)
+      int g = 0;            // ring steps consumed
       bool ok = true;
       for (int k = 0, item = nth_item(0); ok && item < n_items; item = nth_item(++k)) {
         const WorkTile w = work_tile<CAUSAL>(p, item);
         for (int t = 0; t < kTilesPerCta && ok; ++t)
           if (w.n_t[t] > 0) ok = mbar_wait(&q_full[t], qn[t] & 1, abort_flag, p.status);
+        // Ring block of step j: e4m3 uses block g + j for K(j) and g + j - 1 for V(j-1); the
+        // 16-bit ring holds both operands of step j in one stage.
         for (int j = 0; ok && j <= w.n_blocks; ++j) {
-          const int gj = g + j;                                  // this block
-          const int s = gj % ST, r = gj / ST;
-          const int sp = (gj + ST - 1) % ST, rp = (gj - 1) / ST;  // block j-1
-          bool k_ready = false;
-          if (j >= 1) {
-            // V of block j-1: converted to f16 (e4m3) or landed (16-bit)
-            uint64_t* vb = (ELEM == kE4M3) ? &v_ready[sp] : &v_full[sp];
-            if (!mbar_wait(vb, rp & 1, abort_flag, p.status)) {
+          const int gk = (ELEM == kE4M3) ? g + j : g;            // stage of K(j)
+          const int gv = (ELEM == kE4M3) ? g + j - 1 : g;        // stage of V(j-1)
+          const int s = gk % ST, r = gk / ST;
+          const int sv = gv % ST, rv = gv / ST;
+          bool k_ready = ELEM != kE4M3;  // e4m3: K(j) is waited for just before the first QK
+          if constexpr (ELEM == kE4M3) {
+            if (j >= 1 && !mbar_wait(&v_ready[sv], rv & 1, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+          } else {
+            if (!mbar_wait(&in_full[s], r & 1, abort_flag, p.status)) {
               ok = false;
               break;
             }
           }
+          tc_fence_after();
           for (int t = 0; t < kTilesPerCta; ++t) {
             const uint32_t tS = tmem_base + t * 128;
             const uint32_t tO = tmem_base + 256 + t * 128;
@@ -353,20 +389,20 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 break;
               }
               tc_fence_after();
-              const uint64_t dv = dv0 + (uint64_t)((sp * C::V_BYTES) >> 4);
+              const uint64_t dv = dv0 + (uint64_t)((sv * C::V_BYTES) >> 4);
               const uint32_t acc0 = (j - 1 > 0) ? 1u : 0u;
 #pragma unroll
               for (int kk = 0; kk < C::PV_STEPS; ++kk)
                 mma_f16_ts(tO, tS + kk * 8, dv + (uint64_t)((kk * 16 * 128) >> 4), idesc_pv, kk > 0 ? 1u : acc0);
-              mma_commit(&o_done[t]);
+              if (j == w.n_t[t]) mma_commit(&o_full[t]);  // O_t of this work tile complete
               ++pn[t];
             }
-            // V of block j-1 is no longer needed once the MMAs issued so far complete
-            if (t == kTilesPerCta - 1 && j >= 1) mma_commit(&v_empty[sp]);
+            // e4m3: the V stage of block j-1 is free once both P.V MMAs of this step complete
+            if (ELEM == kE4M3 && t == kTilesPerCta - 1 && j >= 1) mma_commit(&v_free[sv]);
             // S_t = Q_t K(j)^T
             if (j < w.n_t[t]) {
               if (!k_ready) {
-                if (!mbar_wait(&k_full[s], r & 1, abort_flag, p.status)) {
+                if (!mbar_wait(&in_full[s], r & 1, abort_flag, p.status)) {
                   ok = false;
                   break;
                 }
@@ -389,10 +425,15 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
               if (j == w.n_t[t] - 1) mma_commit(&q_empty[t]);  // Q_t of this work tile fully used
             }
           }
-          // K of block j is no longer needed once its QK MMAs complete
-          if (ok && j < w.n_blocks) mma_commit(&k_empty[s]);
+          if constexpr (ELEM == kE4M3) {
+            if (ok && j < w.n_blocks) mma_commit(&released[s]);  // K(j) free once its QKs complete
+          } else {
+            // everything this step read from ring stage s is free once these MMAs complete
+            if (ok) mma_commit(&released[s]);
+            ++g;
+          }
         }
-        g += w.n_blocks;
+        if (ELEM == kE4M3) g += w.n_blocks;
         for (int t = 0; t < kTilesPerCta; ++t)
           if (w.n_t[t] > 0) ++qn[t];
       }
@@ -441,7 +482,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const uint32_t tS = tmem_base + lane_off + t * 128;
     const uint32_t tO = tmem_base + lane_off + 256 + t * 128;
     const float scale2 = p.scale2;
-    int sn = 0;  // S blocks consumed (s_full / p_full / o_done phases)
+    int sn = 0;  // S blocks consumed (s_full / p_full phases)
+    int on = 0;  // work tiles finished (o_full phases)
     bool ok = true;
     for (int k = 0, item = nth_item(0); ok && item < n_items; item = nth_item(++k)) {
       const WorkTile w = work_tile<CAUSAL>(p, item);
@@ -562,12 +604,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
         l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         if (rescale && j > 0) {
-          // O holds P.V of blocks < j at the old max: wait for that MMA, then scale it
-          if (!mbar_wait_warp(&o_done[t], (sn - 1) & 1, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+          // O holds P.V of blocks < j at the old max (finished: s_full(j) covers it); scale it
 #pragma unroll 1
           for (int c = 0; c < DV / 32; ++c) {
             uint32_t o[32];
@@ -591,10 +628,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       if (!ok) break;
 
       // ---------------------------------------------------------- epilogue: O / l, LSE
-      if (!mbar_wait_warp(&o_done[t], (sn - 1) & 1, abort_flag, p.status)) {
+      if (!mbar_wait_warp(&o_full[t], on & 1, abort_flag, p.status)) {
         ok = false;
         break;
       }
+      ++on;
       tc_fence_after();
       const float inv = (l > 0.f) ? p.out_scale / l : 0.f;
       uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
