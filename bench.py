@@ -391,6 +391,30 @@ def main_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def profile_run(args):
+    """Launch one workload's kernels warmup + steps times and print their mean time (no L2 flush,
+    no e2e, no CPU baseline): a small, self-contained command for ncu captures."""
+    import flash_attention_forward_gb300 as fa
+
+    fa.library()
+    w = workloads.WORKLOADS[args.profile]
+    if args.batch:
+        w = w.with_shape(B=args.batch)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if w.kind == "decode":
+        x = workloads.decode_inputs(w, pad_value=0.0)
+        q, k, v, kvl = (x[n].to(dev) for n in ("q", "k", "v", "kv_len"))
+        ws = torch.empty(fa.sdpa_decode_workspace_size(w.B, w.Hq, w.Sk, w.Dv), dtype=torch.uint8, device=dev)
+
+        def step(_i=0):
+            fa.sdpa_decode(q, k, v, kvl, scale=w.scale, workspace=ws)
+    else:
+        _, step = prefill_setup(w, dev)
+    ms = time_steps(step, max(args.steps, 1), max(args.warmup, 1))
+    status = fa.sdpa_status_string(fa.sdpa_check_device_status())
+    print(json.dumps({"profile": w.name, "B": w.B, "ms_per_step": sum(ms) / len(ms), "device_status": status}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -399,7 +423,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", metavar="WORKLOAD", help="only run WORKLOAD's launches (for ncu captures)")
+    ap.add_argument("--batch", type=int, default=0, help="with --profile: override the batch size")
     args = ap.parse_args()
+    if args.profile:
+        profile_run(args)
+        return
     args.warmup = max(args.warmup, 3)
     rank, local, world = dist_setup()
     if args.impl == "reference":

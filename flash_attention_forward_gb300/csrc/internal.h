@@ -29,6 +29,7 @@ struct PrefillParams {
   int B, Hq, Hkv, Sq, Sk;
   int group;               // Hq / Hkv
   int n_cta_tiles;         // ceil(Sq / kCtaRows)
+  int units_per_group;     // KV units (batch x KV head) whose work tiles are scheduled together
   int n_kblocks;           // ceil(Sk / kBlockK)
   float scale2;            // scale * log2(e) (times descale_q * descale_k for e4m3)
   float inv_scale;         // 1 / (scale * descale_q * descale_k): mask values enter s in score units

@@ -133,19 +133,30 @@ struct WorkTile {
   int n_blocks;           // blocks streamed for the work tile = max over its query tiles
 };
 
-// Work tiles in launch order.  Causal tiles at the bottom of the matrix see the most keys and
-// come first; within a row band the query heads of one KV group are adjacent, so the CTAs that
-// run them together share K/V through L2.
+// Work tiles in launch order.  A KV unit is one (batch, KV head): its K/V are shared by the
+// Hq/Hkv query heads of the group and all their query tiles.  Units are taken in groups of
+// p.units_per_group (sized on the host so that a group fills whole pairs of snake rounds and its
+// K/V fits in L2), so the K/V that the CTAs running at the same time need stays resident in L2.
+// Inside a group, causal tiles at the bottom of the matrix see the most keys and come first;
+// tiles of one row band are ordered by unit, then query head.
 template <bool CAUSAL>
 __device__ __forceinline__ WorkTile work_tile(const PrefillParams& p, int item) {
   WorkTile w;
-  const int bh_count = p.B * p.Hq;
-  const int bh = item % bh_count;
-  const int rank = item / bh_count;
+  const int G = p.group;                           // query heads per KV head
+  const int units = p.B * p.Hkv;
+  const int per_unit = G * p.n_cta_tiles;          // work tiles of one KV unit
+  const int gsize = p.units_per_group * per_unit;  // work tiles of a full group
+  const int gi = item / gsize;
+  const int base = gi * p.units_per_group;
+  const int ul = min(p.units_per_group, units - base);  // units in this group (last may be short)
+  const int r = item - gi * gsize;
+  const int rank = r / (ul * G);                   // row band, longest first when causal
+  const int q = r - rank * (ul * G);
+  const int unit = base + q / G;
   const int ctile = CAUSAL ? (p.n_cta_tiles - 1 - rank) : rank;
-  w.b = bh / p.Hq;
-  w.h = bh % p.Hq;
-  w.kvh = w.h / p.group;
+  w.b = unit / p.Hkv;
+  w.kvh = unit % p.Hkv;
+  w.h = w.kvh * G + q % G;
   w.q0 = ctile * kCtaRows;
   w.n_blocks = 0;
 #pragma unroll

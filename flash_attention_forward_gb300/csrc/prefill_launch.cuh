@@ -19,7 +19,20 @@ cudaError_t launch_prefill_instance(const CUtensorMap& tq, const CUtensorMap& tk
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const long long items = (long long)p.n_cta_tiles * p.B * p.Hq;
   const unsigned grid = (unsigned)(items < sms ? items : sms);
-  kern<<<grid, kPrefillThreads, C::SMEM, st>>>(tq, tk, tv, p);
+  // Group KV units so that a group is a whole number of snake round pairs (2 x grid work
+  // tiles; the snake balances inside it) and its K/V stays within a 64 MiB share of L2.
+  PrefillParams q = p;
+  const long long per_unit = (long long)p.n_cta_tiles * p.group;
+  const long long two_rounds = 2LL * grid;
+  long long a = per_unit, b = two_rounds;
+  while (b) { const long long t = a % b; a = b; b = t; }          // gcd(per_unit, 2 x grid)
+  const long long aligned = two_rounds / a;
+  const long long kv_unit_bytes = (long long)p.Sk * (D * C::ESZ + DV * C::ESZ);
+  const long long cap = (64LL << 20) / (kv_unit_bytes > 0 ? kv_unit_bytes : 1);
+  long long ug = aligned < cap ? aligned : cap;
+  const long long units = (long long)p.B * p.Hkv;
+  q.units_per_group = (int)(ug < 1 ? 1 : (ug > units ? units : ug));
+  kern<<<grid, kPrefillThreads, C::SMEM, st>>>(tq, tk, tv, q);
   return cudaGetLastError();
 }
 
