@@ -10,13 +10,14 @@
 
 namespace sdpa {
 namespace {
-
 __device__ uint32_t g_status_word;
+}  // namespace
 
 constexpr int kMaxDevices = 64;
 uint32_t* g_status_ptr[kMaxDevices] = {};
 std::mutex g_mu;
 
+namespace {
 // Device address of this device's status word (looked up once per device).
 cudaError_t status_ptr(uint32_t** out) {
   int dev = 0;
@@ -52,8 +53,10 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Tensor map of a [B, S, H, Dh] tensor (element strides sb, ss, sh; innermost stride 1),
-// box = box0 x 1 x box_rows x 1.
+}  // namespace
+
+cudaError_t device_status_ptr(uint32_t** out) { return status_ptr(out); }
+
 bool encode_bshd(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int esize, int B, int S, int H, int Dh,
                  int64_t sb, int64_t ss, int64_t sh, int box0, int box_rows, CUtensorMapSwizzle sw) {
   EncodeTiledFn fn = encode_fn();
@@ -65,6 +68,8 @@ bool encode_bshd(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int
   return fn(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -250,15 +255,25 @@ int sdpa_decode(const void* q, const void* k_cache, const void* v_cache, const i
   if (!workspace || !aligned16(workspace) || workspace_bytes < sdpa_decode_workspace_size(B, Hq, max_kv, Dv))
     return SDPA_ERR_INVALID;
 
+  const CUtensorMapDataType dt = dtype == SDPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  alignas(64) CUtensorMap tk, tv;
+  if (!encode_bshd(&tk, k_cache, dt, 2, B, max_kv, Hkv, D, st[2], st[3], st[4], 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_bshd(&tv, v_cache, dt, 2, B, max_kv, Hkv, Dv, st[5], st[6], st[7], 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+    return SDPA_ERR_CUDA;
+  uint32_t* status = nullptr;
+  if (status_ptr(&status) != cudaSuccess) return SDPA_ERR_CUDA;
+
   DecodeParams p{};
   p.q = q, p.k = k_cache, p.v = v_cache, p.kv_len = kv_len, p.o = o, p.lse = lse;
   p.ws = static_cast<float*>(workspace);
+  p.status = status;
   p.q_b = st[0], p.q_h = st[1], p.k_b = st[2], p.k_s = st[3], p.k_h = st[4];
   p.v_b = st[5], p.v_s = st[6], p.v_h = st[7], p.o_b = st[8], p.o_h = st[9];
   p.B = B, p.Hq = Hq, p.Hkv = Hkv, p.max_kv = max_kv, p.group = group;
   p.n_splits_max = (max_kv + kDecodeSplit - 1) / kDecodeSplit;
   p.scale2 = (float)((double)scale * 1.4426950408889634);
-  const cudaError_t e = launch_decode(dtype == SDPA_BF16 ? kBF16 : kF16, p, static_cast<cudaStream_t>(stream));
+  const cudaError_t e =
+      launch_decode(dtype == SDPA_BF16 ? kBF16 : kF16, p, tk, tv, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 

@@ -75,161 +75,231 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return d;
 }
 
-// Thread layout inside a warp (m16n8k16 fragments): g = lane / 4 is the query head of the
-// group for A/C rows and the key (QK) or value column (PV) for B; t = lane % 4.
+// Phase 1 layout.  A CTA is 4 consumer warps plus one producer warp.  The producer streams the
+// split's keys in chunks of kDecChunk rows: two 64-column TMA boxes of K and two of V per chunk
+// (128-byte swizzle) into a kDecStages-deep shared-memory ring.  Consumer warp w takes rows
+// [16 w, 16 w + 16) of every chunk, copies its fragments to registers and releases the stage at
+// once.
 //
-// The head dimension is permuted consistently for Q and K, so that each thread's B operand
-// for the 8 QK k-steps is exactly four 16-byte loads of its key row: thread t owns dims
-// [32 i + 8 t, 32 i + 8 t + 8) for i = 0..3, k-step kk uses chunk i = kk / 2, words 2 (kk%2)
-// (virtual k 2t, 2t+1) and 2 (kk%2) + 1 (virtual k 2t+8, 2t+9).  A dot product does not
-// depend on the order of its terms, so S is unchanged.
-//
-// The value dimension is permuted too: PV n-tile nt, column g holds value dim 16 g + nt, so
-// each thread's B operand for all 16 n-tiles is one 32-byte run of a value row, and the C
-// fragment of thread (g, t) ends up holding value dims [32 t, 32 t + 32) of query head g.
+// Fragments (m16n8k16): g = lane / 4 is the query head of the group for A/C rows and the key
+// (QK) or value column (PV) for B; t = lane % 4.
+//  * Head dimension, permuted consistently for Q and K: thread t owns dims [32 i + 8 t, +8)
+//    for i = 0..3; k-step kk uses chunk i = kk / 2, words 2 (kk%2) and 2 (kk%2) + 1.  A dot
+//    product does not depend on the order of its terms.
+//  * Keys: QK n-index n of n-tile nt is key 8 nt + kSigma[n] of the warp's 16, and P.V k-index
+//    k is the same key as QK's (nt, n) = (k / 8, k % 8).  Any fixed order of keys gives the
+//    same softmax; this one spreads the eight rows a quarter-warp reads over all swizzle phases.
+//  * Value dims: P.V n-tile nt, column g is value dim 16 kBeta[g] + nt, so each thread's B
+//    operand for all 16 n-tiles is one 32-byte run of a value row; the C fragment of thread
+//    (g, t) ends up holding value dims 16 kBeta[2t] + nt and 16 kBeta[2t + 1] + nt.
+constexpr int kDecChunk = 64;                           // keys per TMA chunk
+constexpr int kDecStages = 3;
+constexpr int kDecBox = kDecChunk * 64 * 2;             // one 64-column box of 16-bit rows: 8 KB
+constexpr int kDecStageBytes = 4 * kDecBox;             // K (2 boxes) + V (2 boxes)
+constexpr int kDecSmem = kDecStages * kDecStageBytes + 256 + 1024;
+constexpr int kDecThreads = (kDecodeWarps + 1) * 32;
+__constant__ int kSigma[8] = {0, 4, 1, 5, 2, 6, 3, 7};
+__constant__ int kBeta[8] = {0, 2, 1, 3, 4, 6, 5, 7};
+
+// byte offset of the 16-byte unit `unit` (0..7) of row `row` in a 128-byte-swizzled box
+__device__ __forceinline__ uint32_t swz(int row, int unit) {
+  return static_cast<uint32_t>(row * 128 + ((unit ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+
 template <int ELEM>
-__global__ void __launch_bounds__(kDecodeWarps * 32) decode_split_kernel(const DecodeParams p) {
-  constexpr int kWarpKeys = kDecodeSplit / kDecodeWarps;
+__global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                                                   const __grid_constant__ CUtensorMap tm_v,
+                                                                   const DecodeParams p) {
+  extern __shared__ uint8_t dsmem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kDecStages * kDecStageBytes);
+  uint64_t* empty = full + kDecStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kDecStages);
+
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
   const int L = min(max(__ldg(p.kv_len + b), 0), p.max_kv);
   const int start = split * kDecodeSplit;
   if (start >= L) return;
-  const int w_begin = start + warp * kWarpKeys;
-  const int w_end = min(w_begin + kWarpKeys, L);
-  const int G = p.group;
-  const float scale2 = p.scale2;
+  const int end = min(start + kDecodeSplit, L);
+  const int nchunks = (end - start + kDecChunk - 1) / kDecChunk;
 
-  uint32_t qf[4][4];
-  if (g < G) {
-    const uint16_t* qrow = reinterpret_cast<const uint16_t*>(p.q) + b * p.q_b + (int64_t)(kvh * G + g) * p.q_h;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 v = ldg128(qrow + 32 * i + 8 * t);
-      qf[i][0] = v.x, qf[i][1] = v.y, qf[i][2] = v.z, qf[i][3] = v.w;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kDecStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kDecodeWarps);
     }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) qf[i][0] = qf[i][1] = qf[i][2] = qf[i][3] = 0u;
+    *abort_flag = 0;
+    fence_mbar_init();
   }
-
-  float acc[16][4];
-#pragma unroll
-  for (int nt = 0; nt < 16; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-  float m = -INFINITY, l = 0.f;
-
-  const uint16_t* kb = reinterpret_cast<const uint16_t*>(p.k) + b * p.k_b + (int64_t)kvh * p.k_h;
-  const uint16_t* vb = reinterpret_cast<const uint16_t*>(p.v) + b * p.v_b + (int64_t)kvh * p.v_h;
-  const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
-
-  for (int t0 = w_begin; t0 < w_end; t0 += 16) {
-    // keys t0 + g and t0 + 8 + g: four 16-byte pieces each (never past w_end)
-    uint4 kr[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      const int tok = t0 + 8 * nt + g;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        kr[nt][i] = zero4;
-        if (tok < w_end) kr[nt][i] = ldg128(kb + (int64_t)tok * p.k_s + 32 * i + 8 * t);
-      }
-    }
-    // values of keys t0 + {2t, 2t+1, 2t+8, 2t+9}, dims [16 g, 16 g + 16)
-    uint4 vr[4][2];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int tok = t0 + 2 * t + (u & 1) + 8 * (u >> 1);
-      const uint16_t* vp = vb + (int64_t)tok * p.v_s + 16 * g;
-      vr[u][0] = zero4;
-      vr[u][1] = zero4;
-      if (tok < w_end) {
-        vr[u][0] = ldg128(vp);
-        vr[u][1] = ldg128(vp + 8);
-      }
-    }
-    // S = Q K^T for 16 keys
-    float sc[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const int i = kk >> 1, hs = kk & 1;
-        mma16816<ELEM>(sc[nt], qf[i][2 * hs], qf[i][2 * hs + 1], word(kr[nt][i], 2 * hs), word(kr[nt][i], 2 * hs + 1));
-      }
-    }
-    float x[4] = {sc[0][0] * scale2, sc[0][1] * scale2, sc[1][0] * scale2, sc[1][1] * scale2};
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int tok = t0 + 2 * t + (u & 1) + 8 * (u >> 1);
-      if (tok >= w_end) x[u] = -INFINITY;
-    }
-    float mb = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
-    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
-    const float m_cand = fmaxf(m, mb);
-    if (__any_sync(0xffffffffu, m_cand > m + kDecodeRescaleLog2)) {
-      const float alpha = (m_cand == -INFINITY) ? 1.f : ex2(m - m_cand);
-      l *= alpha;
-#pragma unroll
-      for (int nt = 0; nt < 16; ++nt) acc[nt][0] *= alpha, acc[nt][1] *= alpha;
-      m = m_cand;
-    }
-    const float neg_m = (m == -INFINITY) ? 0.f : -m;
-    const uint32_t a0 = pack2<ELEM>(ex2(x[0] + neg_m), ex2(x[1] + neg_m));
-    const uint32_t a2 = pack2<ELEM>(ex2(x[2] + neg_m), ex2(x[3] + neg_m));
-    l += sum2<ELEM>(a0) + sum2<ELEM>(a2);
-    // O += P V over the 16 keys, 16 n-tiles of 8 (permuted) value columns
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      const int wi = (nt & 7) >> 1, hv = nt >> 3;
-      const uint32_t sel = (nt & 1) ? 0x7632u : 0x5410u;
-      const uint32_t b0 = prmt(word(vr[0][hv], wi), word(vr[1][hv], wi), sel);
-      const uint32_t b1 = prmt(word(vr[2][hv], wi), word(vr[3][hv], wi), sel);
-      mma16816<ELEM>(acc[nt], a0, a2, b0, b1);
-    }
-  }
-
-  // per-row sum over the four threads sharing a query head
-  l += __shfl_xor_sync(0xffffffffu, l, 1);
-  l += __shfl_xor_sync(0xffffffffu, l, 2);
+  __syncthreads();
 
   __shared__ float sm_m[kDecodeWarps][8];
   __shared__ float sm_l[kDecodeWarps][8];
-  __shared__ float sm_o[kDecodeWarps][8][kDecodeDv];
-  if (g < G) {
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      sm_o[warp][g][32 * t + nt] = acc[nt][0];
-      sm_o[warp][g][32 * t + 16 + nt] = acc[nt][1];
+  const int G = p.group;
+
+  if (warp == kDecodeWarps) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      int c = 0;
+      for (; c < nchunks; ++c) {
+        const int s = c % kDecStages, r = c / kDecStages;
+        if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, abort_flag, p.status)) break;
+        uint8_t* st = smem + s * kDecStageBytes;
+        const int row = start + c * kDecChunk;  // rows past max_kv read as zeros
+        mbar_arrive_expect_tx(&full[s], kDecStageBytes);
+        tma_load_4d(st, &tm_k, &full[s], 0, kvh, row, b);
+        tma_load_4d(st + kDecBox, &tm_k, &full[s], 64, kvh, row, b);
+        tma_load_4d(st + 2 * kDecBox, &tm_v, &full[s], 0, kvh, row, b);
+        tma_load_4d(st + 3 * kDecBox, &tm_v, &full[s], 64, kvh, row, b);
+      }
+      if (c < nchunks)  // aborted: let the copies in flight land
+        for (int j = max(0, c - kDecStages); j < c; ++j) mbar_drain(&full[j % kDecStages], (j / kDecStages) & 1);
     }
-    if (t == 0) {
-      sm_m[warp][g] = m;
-      sm_l[warp][g] = l;
-    }
-  }
-  __syncthreads();
-  const int n_splits = p.n_splits_max;
-  const int dv = threadIdx.x;  // kDecodeWarps * 32 == kDecodeDv
-  for (int r = 0; r < G; ++r) {
-    float M = -INFINITY;
+  } else {
+    // ---------------------------------------------------------- consumers
+    const int g = lane >> 2, t = lane & 3;
+    const float scale2 = p.scale2;
+    uint32_t qf[4][4];
+    if (g < G) {
+      const uint16_t* qrow = reinterpret_cast<const uint16_t*>(p.q) + b * p.q_b + (int64_t)(kvh * G + g) * p.q_h;
 #pragma unroll
-    for (int wi = 0; wi < kDecodeWarps; ++wi) M = fmaxf(M, sm_m[wi][r]);
-    float o = 0.f, ls = 0.f;
+      for (int i = 0; i < 4; ++i) {
+        const uint4 v = ldg128(qrow + 32 * i + 8 * t);
+        qf[i][0] = v.x, qf[i][1] = v.y, qf[i][2] = v.z, qf[i][3] = v.w;
+      }
+    } else {
 #pragma unroll
-    for (int wi = 0; wi < kDecodeWarps; ++wi) {
-      const float mw = sm_m[wi][r];
-      const float e = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-      o += e * sm_o[wi][r][dv];
-      ls += e * sm_l[wi][r];
+      for (int i = 0; i < 4; ++i) qf[i][0] = qf[i][1] = qf[i][2] = qf[i][3] = 0u;
     }
-    const int h = kvh * G + r;
-    float* part = p.ws + ((int64_t)(b * p.Hq + h) * n_splits + split) * (kDecodeDv + 2);
-    part[dv] = o;
-    if (dv == 0) {
-      part[kDecodeDv] = M;
-      part[kDecodeDv + 1] = ls;
+    const int beta_g = kBeta[g];
+    int sig_k[2], sig_v[4];  // chunk rows of this thread's K (per n-tile) and V (per u) keys
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) sig_k[nt] = 16 * warp + 8 * nt + kSigma[g];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) sig_v[u] = 16 * warp + 8 * (u >> 1) + kSigma[2 * t + (u & 1)];
+
+    float acc[16][4];
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+
+    for (int c = 0; c < nchunks; ++c) {
+      const int s = c % kDecStages;
+      if (!mbar_wait_warp(&full[s], (c / kDecStages) & 1, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      const uint8_t* kS = smem + s * kDecStageBytes;
+      const uint8_t* vS = kS + 2 * kDecBox;
+      const int row0 = start + c * kDecChunk;  // key index of chunk row 0
+      uint4 kr[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) kr[nt][i] = lds128(kS + (i >> 1) * kDecBox + swz(sig_k[nt], (i & 1) * 4 + t));
+      uint4 vr[4][2];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const bool valid = row0 + sig_v[u] < end;  // rows past kv_len may hold anything (NaN)
+#pragma unroll
+        for (int hv = 0; hv < 2; ++hv) {
+          const uint4 x = lds128(vS + (beta_g >> 2) * kDecBox + swz(sig_v[u], 2 * (beta_g & 3) + hv));
+          vr[u][hv] = valid ? x : make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);  // fragments are in registers: the stage may refill
+
+      // S = Q K^T for this warp's 16 keys of the chunk
+      float sc[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const int i = kk >> 1, hs = kk & 1;
+          mma16816<ELEM>(sc[nt], qf[i][2 * hs], qf[i][2 * hs + 1], word(kr[nt][i], 2 * hs), word(kr[nt][i], 2 * hs + 1));
+        }
+      }
+      float x[4] = {sc[0][0] * scale2, sc[0][1] * scale2, sc[1][0] * scale2, sc[1][1] * scale2};
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (row0 + sig_v[u] >= end) x[u] = -INFINITY;  // (nt, n) = (u / 2, 2t + u % 2): same key as V row u
+      float mb = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+      const float m_cand = fmaxf(m, mb);
+      if (__any_sync(0xffffffffu, m_cand > m + kDecodeRescaleLog2)) {
+        const float alpha = (m_cand == -INFINITY) ? 1.f : ex2(m - m_cand);
+        l *= alpha;
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) acc[nt][0] *= alpha, acc[nt][1] *= alpha;
+        m = m_cand;
+      }
+      const float neg_m = (m == -INFINITY) ? 0.f : -m;
+      const uint32_t a0 = pack2<ELEM>(ex2(x[0] + neg_m), ex2(x[1] + neg_m));
+      const uint32_t a2 = pack2<ELEM>(ex2(x[2] + neg_m), ex2(x[3] + neg_m));
+      l += sum2<ELEM>(a0) + sum2<ELEM>(a2);
+      // O += P V over the 16 keys, 16 n-tiles of 8 (permuted) value columns
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        const int wi = (nt & 7) >> 1, hv = nt >> 3;
+        const uint32_t sel = (nt & 1) ? 0x7632u : 0x5410u;
+        const uint32_t b0 = prmt(word(vr[0][hv], wi), word(vr[1][hv], wi), sel);
+        const uint32_t b1 = prmt(word(vr[2][hv], wi), word(vr[3][hv], wi), sel);
+        mma16816<ELEM>(acc[nt], a0, a2, b0, b1);
+      }
+    }
+
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    if (!ok) {
+      m = -INFINITY;
+      l = 0.f;
+    }
+    // merge the four warps: per-warp O goes to the (now idle) ring memory
+    __syncwarp();
+    asm volatile("bar.sync 1, %0;" ::"n"(kDecodeWarps * 32));  // all consumers are past the ring
+    float* sm_o = reinterpret_cast<float*>(smem);               // [warp][row][dv]
+    if (g < G) {
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        sm_o[(warp * 8 + g) * kDecodeDv + 16 * kBeta[2 * t] + nt] = acc[nt][0];
+        sm_o[(warp * 8 + g) * kDecodeDv + 16 * kBeta[2 * t + 1] + nt] = acc[nt][1];
+      }
+      if (t == 0) {
+        sm_m[warp][g] = m;
+        sm_l[warp][g] = l;
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kDecodeWarps * 32));
+    const int n_splits = p.n_splits_max;
+    const int dv = threadIdx.x;  // kDecodeWarps * 32 == kDecodeDv
+    for (int r = 0; r < G; ++r) {
+      float M = -INFINITY;
+#pragma unroll
+      for (int wi = 0; wi < kDecodeWarps; ++wi) M = fmaxf(M, sm_m[wi][r]);
+      float o = 0.f, ls = 0.f;
+#pragma unroll
+      for (int wi = 0; wi < kDecodeWarps; ++wi) {
+        const float mw = sm_m[wi][r];
+        const float e = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+        o += e * sm_o[(wi * 8 + r) * kDecodeDv + dv];
+        ls += e * sm_l[wi][r];
+      }
+      const int h = kvh * G + r;
+      float* part = p.ws + ((int64_t)(b * p.Hq + h) * n_splits + split) * (kDecodeDv + 2);
+      part[dv] = o;
+      if (dv == 0) {
+        part[kDecodeDv] = M;
+        part[kDecodeDv + 1] = ls;
+      }
     }
   }
 }
@@ -290,13 +360,21 @@ __global__ void __launch_bounds__(128) mask_convert_kernel(const MaskConvertPara
 
 }  // namespace
 
-cudaError_t launch_decode(int elem, const DecodeParams& p, cudaStream_t st) {
+cudaError_t launch_decode(int elem, const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                          cudaStream_t st) {
   const dim3 g1(p.n_splits_max, p.Hkv, p.B), g2(p.Hq, p.B);
+  cudaError_t e;
   if (elem == kBF16) {
-    decode_split_kernel<kBF16><<<g1, kDecodeWarps * 32, 0, st>>>(p);
+    if ((e = cudaFuncSetAttribute(decode_split_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kDecSmem)) != cudaSuccess)
+      return e;
+    decode_split_kernel<kBF16><<<g1, kDecThreads, kDecSmem, st>>>(tk, tv, p);
     decode_combine_kernel<kBF16><<<g2, kDecodeDv, 0, st>>>(p);
   } else {
-    decode_split_kernel<kF16><<<g1, kDecodeWarps * 32, 0, st>>>(p);
+    if ((e = cudaFuncSetAttribute(decode_split_kernel<kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kDecSmem)) != cudaSuccess)
+      return e;
+    decode_split_kernel<kF16><<<g1, kDecThreads, kDecSmem, st>>>(tk, tv, p);
     decode_combine_kernel<kF16><<<g2, kDecodeDv, 0, st>>>(p);
   }
   return cudaGetLastError();

@@ -88,17 +88,25 @@ extern "C" int sdpa_decode_noalloc(const void* q, const void* k_cache, const voi
   if (reinterpret_cast<uintptr_t>(kv_len) & 3u) return SDPA_ERR_INVALID;
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SDPA_ERR_INVALID;
 
+  const CUtensorMapDataType dt = dtype == SDPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  alignas(64) CUtensorMap tk, tv;
+  if (!encode_bshd(&tk, k_cache, dt, 2, B, max_kv, Hkv, D, st[2], st[3], st[4], 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_bshd(&tv, v_cache, dt, 2, B, max_kv, Hkv, Dv, st[5], st[6], st[7], 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+    return SDPA_ERR_CUDA;
   float* scratch = nullptr;
-  if (noalloc_scratch(&scratch) != cudaSuccess) return SDPA_ERR_CUDA;
+  uint32_t* status = nullptr;
+  if (noalloc_scratch(&scratch) != cudaSuccess || device_status_ptr(&status) != cudaSuccess) return SDPA_ERR_CUDA;
 
   DecodeParams p{};
   p.q = q, p.k = k_cache, p.v = v_cache, p.kv_len = kv_len, p.o = o, p.lse = lse;
   p.ws = scratch;
+  p.status = status;
   p.q_b = st[0], p.q_h = st[1], p.k_b = st[2], p.k_s = st[3], p.k_h = st[4];
   p.v_b = st[5], p.v_s = st[6], p.v_h = st[7], p.o_b = st[8], p.o_h = st[9];
   p.B = B, p.Hq = Hq, p.Hkv = Hkv, p.max_kv = max_kv, p.group = group;
   p.n_splits_max = (int)n_splits;
   p.scale2 = (float)((double)scale * 1.4426950408889634);
-  const cudaError_t e = launch_decode(dtype == SDPA_BF16 ? kBF16 : kF16, p, static_cast<cudaStream_t>(stream));
+  const cudaError_t e =
+      launch_decode(dtype == SDPA_BF16 ? kBF16 : kF16, p, tk, tv, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }

@@ -50,6 +50,7 @@ struct DecodeParams {
   void* o;
   float* lse;
   float* ws;               // [B, Hq, n_splits_max, Dv + 2]
+  uint32_t* status;        // device status word
   int64_t q_b, q_h, k_b, k_s, k_h, v_b, v_s, v_h, o_b, o_h;
   int B, Hq, Hkv, max_kv, group, n_splits_max;
   float scale2;            // scale * log2(e)
@@ -78,7 +79,16 @@ cudaError_t launch_prefill_bf16(int D, int Dv, bool causal, bool has_mask, const
 cudaError_t launch_prefill_e4m3(int D, int Dv, bool causal, bool has_mask, const CUtensorMap& tq,
                                 const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st,
                                 bool* supported);
-cudaError_t launch_decode(int elem, const DecodeParams& p, cudaStream_t st);
+cudaError_t launch_decode(int elem, const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                          cudaStream_t st);
+
+// Device address of the current device's status word.
+cudaError_t device_status_ptr(uint32_t** out);
+
+// Tensor map of a [B, S, H, Dh] tensor (element strides sb, ss, sh; innermost stride 1) with a
+// box of box0 x 1 x box_rows x 1 elements; false if the driver rejects it.
+bool encode_bshd(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int esize, int B, int S, int H, int Dh,
+                 int64_t sb, int64_t ss, int64_t sh, int box0, int box_rows, CUtensorMapSwizzle sw);
 cudaError_t launch_mask_convert(const MaskConvertParams& p, cudaStream_t st);
 
 }  // namespace sdpa

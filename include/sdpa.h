@@ -118,7 +118,9 @@ size_t sdpa_decode_workspace_size(int B, int Hq, int max_kv, int Dv);
  * sdpa_decode -- two-phase split-KV decode: one query token per (b, query head) against
  * the first kv_len[b] rows of a padded K/V cache.  Phase 1 gives every (b, kv head,
  * split of keys) a partial (O, m, l); phase 2 merges the splits of a (b, q head) with a
- * log-sum-exp combine.  Cache rows at or beyond kv_len[b] are never read.
+ * log-sum-exp combine.  Cache rows at or beyond kv_len[b] never contribute (they may hold
+ * anything, NaN included); keys stream in 64-row chunks, so up to 63 such rows may be read,
+ * never past max_kv.
  * (page "Xe2 ESIMD Flash Attention", section "Assets": two-phase full-dense decode)
  *
  *   q       [B, Hq, D]                 dtype            o   [B, Hq, Dv]  dtype (written)
