@@ -3,6 +3,7 @@
 // device memory; every argument is checked before the first CUDA call.
 #include <cmath>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "sdpa.h"
@@ -18,6 +19,8 @@ uint32_t* g_status_ptr[kMaxDevices] = {};
 std::mutex g_mu;
 
 namespace {
+std::atomic<int> g_stall_next{0};
+
 // Device address of this device's status word (looked up once per device).
 cudaError_t status_ptr(uint32_t** out) {
   int dev = 0;
@@ -167,6 +170,7 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   p.inv_scale = (float)(1.0 / s_eff);
   p.out_scale = descale_v;
   p.status = status;
+  p.stall_first_stage = g_stall_next.exchange(0);
   if (mask) {
     const size_t rows = (size_t)B * (size_t)Sq;
     uint4* bits = static_cast<uint4*>(workspace);
@@ -299,5 +303,10 @@ const char* sdpa_status_string(int status) {
 }
 
 int sdpa_version(void) { return 100; }
+
+int sdpa_debug_stall_next_call(void) {
+  g_stall_next.store(1);
+  return SDPA_OK;
+}
 
 }  // extern "C"

@@ -40,6 +40,7 @@ struct PrefillParams {
   const uint16_t* mask;    // original fp16 mask, read only for flagged block rows
   int64_t mask_b, mask_i;  // element strides of the original mask
   uint32_t* status;        // device status word
+  int stall_first_stage;   // test hook: the producer never fills the first K/V stage
 };
 
 struct DecodeParams {

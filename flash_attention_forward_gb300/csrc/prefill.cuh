@@ -295,6 +295,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
               ok = false;
               break;
             }
+            if (p.stall_first_stage && g == 0) continue;  // test hook: stage 0 never fills
             mbar_arrive_expect_tx(&in_full[s], C::K_BYTES);
             for (int c = 0; c < C::NCH_D; ++c)
               tma_load_4d(sK + s * C::K_BYTES + c * kBlockK * C::CHB, &tm_k, &in_full[s], c * C::CH, w.kvh,
@@ -316,6 +317,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             ok = false;
             break;
           }
+          if (p.stall_first_stage && g == 0) continue;  // test hook: stage 0 never fills
           constexpr uint32_t v_bytes = (ELEM == kE4M3) ? C::VRAW_BYTES : C::V_BYTES;
           mbar_arrive_expect_tx(&in_full[s], (has_k ? C::K_BYTES : 0) + (has_v ? v_bytes : 0));
           if (has_k) {

@@ -177,6 +177,16 @@ const char* sdpa_status_string(int status);
 /* Library version: major * 10000 + minor * 100 + patch. */
 int sdpa_version(void);
 
+/*
+ * sdpa_debug_stall_next_call -- test hook for the failure path.  Arms a one-shot flag
+ * (process-wide): the next sdpa_fwd / sdpa_fwd_fp8 launch withholds its first K/V stage, so
+ * every CTA's bounded waits give up after about one second, the CTAs drain their copies,
+ * free tensor memory and exit, and sdpa_check_device_status() then returns
+ * SDPA_ERR_TIMEOUT.  The CUDA context stays usable.  Returns SDPA_OK.  Nothing in the
+ * library calls it.
+ */
+int sdpa_debug_stall_next_call(void);
+
 #ifdef __cplusplus
 }
 #endif
