@@ -86,20 +86,13 @@ __device__ __forceinline__ uint32_t pack_p(float lo, float hi) {
     return pack_f16x2(lo, hi);
 }
 
+// (acc0, acc1) += the two rounded probabilities packed in w, exactly as the P.V product sees them
 template <int ELEM>
-__device__ __forceinline__ float p_lo(uint32_t w) {
+__device__ __forceinline__ void acc_p_pair(float& acc0, float& acc1, uint32_t w) {
   if constexpr (ELEM == kBF16)
-    return bf16lo_f32(w);
+    add_bf16x2_to_f32(acc0, acc1, w);
   else
-    return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu)));
-}
-
-template <int ELEM>
-__device__ __forceinline__ float p_hi(uint32_t w) {
-  if constexpr (ELEM == kBF16)
-    return bf16hi_f32(w);
-  else
-    return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+    add_f16x2_to_f32(acc0, acc1, w);
 }
 
 // Output element packing (bf16 unless the inputs are f16).
@@ -608,9 +601,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
               ffma2_scalar(x0, x1, s[c], s[c + 1], scale2, neg_m);
               pk[w2] = pack_p<ELEM>(ex2(x0), ex2(x1));
               if (w2 & 1)
-                fadd2(ls[2], ls[3], p_lo<ELEM>(pk[w2]), p_hi<ELEM>(pk[w2]));
+                acc_p_pair<ELEM>(ls[2], ls[3], pk[w2]);
               else
-                fadd2(ls[0], ls[1], p_lo<ELEM>(pk[w2]), p_hi<ELEM>(pk[w2]));
+                acc_p_pair<ELEM>(ls[0], ls[1], pk[w2]);
             }
             tmem_st32(tS + half * 32, pk);
           }
