@@ -23,6 +23,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -75,11 +76,20 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+def _code_only(text: str) -> str:
+    """Source text without // and /* */ comments and with whitespace collapsed, so that edits to
+    comments do not count as kernel changes (the kernel sources hold no string literal with //)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def source_sha() -> str:
+    """Hash of the kernel sources' code (comments and whitespace ignored)."""
     h = hashlib.sha256()
     for p in sorted(glob.glob(os.path.join(ROOT, "flash_attention_forward_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode() + f.read())
+        with open(p, encoding="utf-8") as f:
+            h.update(os.path.basename(p).encode() + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -2,11 +2,12 @@
 // that condenses an fp16 additive mask for the prefill kernels.
 //
 // Phase 1 (decode_split_kernel): a CTA owns one (sequence b, KV head, split of
-// kDecodeSplit keys); its four warps stream disjoint quarters of the split straight from
-// HBM with 128-bit loads.  All Hq/Hkv query heads of the KV head ride in the rows of one
-// m16n8k16 tensor-core tile, so every K/V byte is read once per KV head.  Each warp runs
-// the online softmax over its keys (running max, lazy rescale, running sum), the four
-// warps merge in shared memory, and the CTA writes one partial (unnormalised O, max, sum).
+// kDecodeSplit keys).  A producer warp streams the split's K and V rows with TMA into a
+// shared-memory ring; four consumer warps each take a quarter of every chunk.  All Hq/Hkv
+// query heads of the KV head ride in the rows of one m16n8k16 tensor-core tile, so every
+// K/V byte is read from HBM once.  Each warp runs the online softmax over its keys (running
+// max, lazy rescale, running sum), the four warps merge in shared memory, and the CTA
+// writes one partial (unnormalised O, max, sum).
 // Phase 2 (decode_combine_kernel): per (b, query head) the partials of all splits are
 // merged with a log-sum-exp weighting and normalised.
 // (page "Xe2 ESIMD Flash Attention - SDP Prefill & Decode", section "Assets": the
