@@ -347,11 +347,15 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           make_idesc(ElemTraits<ELEM>::qk_fmt, ElemTraits<ELEM>::qk_fmt, 0, 0, kBlockQ, kBlockK);
       constexpr uint32_t idesc_pv = make_idesc(ElemTraits<ELEM>::pv_fmt, ElemTraits<ELEM>::pv_fmt, 0, 1, kBlockQ, DV);
       // Descriptors are built once; a k-step or stage only moves the start address, whose
-      // field holds (address >> 4) in the low 14 bits, so an add of (offset >> 4) is exact
-      // for shared addresses below 256 KB.
+      // field holds (address >> 4) in the low 14 bits of the low word.  For shared addresses
+      // below 256 KB an add of (offset >> 4) to the low word is exact and never carries out
+      // of the field, so the high words stay fixed.
       const uint64_t dq0 = make_smem_desc(smem_u32(sQ), 16, 8 * C::CHB, C::SW);
       const uint64_t dk0 = make_smem_desc(smem_u32(sK), 16, 8 * C::CHB, C::SW);
       const uint64_t dv0 = make_smem_desc(smem_u32(sV), kBlockK * 128, 1024, kSwizzle128B);
+      const uint32_t q_lo = static_cast<uint32_t>(dq0), q_hi = static_cast<uint32_t>(dq0 >> 32);
+      const uint32_t k_lo = static_cast<uint32_t>(dk0), k_hi = static_cast<uint32_t>(dk0 >> 32);
+      const uint32_t v_lo = static_cast<uint32_t>(dv0), v_hi = static_cast<uint32_t>(dv0 >> 32);
       int qn[2] = {0, 0};   // work tiles seen per tile slot (q_full / q_empty / o_full / o_empty phases)
       int pn[2] = {0, 0};   // P.V blocks issued per tile slot (p_full phases)
       int g = 0;            // ring steps consumed
@@ -395,11 +399,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 break;
               }
               tc_fence_after();
-              const uint64_t dv = dv0 + (uint64_t)((sv * C::V_BYTES) >> 4);
+              const uint32_t dv = v_lo + static_cast<uint32_t>((sv * C::V_BYTES) >> 4);
               const uint32_t acc0 = (j - 1 > 0) ? 1u : 0u;
 #pragma unroll
               for (int kk = 0; kk < C::PV_STEPS; ++kk)
-                mma_f16_ts(tO, tS + kk * 8, dv + (uint64_t)((kk * 16 * 128) >> 4), idesc_pv, kk > 0 ? 1u : acc0);
+                mma_f16_ts(tO, tS + kk * 8, dv + static_cast<uint32_t>((kk * 16 * 128) >> 4), v_hi, idesc_pv, kk > 0 ? 1u : acc0);
               if (j == w.n_t[t]) mma_commit(&o_full[t]);  // O_t of this work tile complete
               ++pn[t];
             }
@@ -415,17 +419,17 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 tc_fence_after();
                 k_ready = true;
               }
-              const uint64_t dq = dq0 + (uint64_t)((t * C::Q_BYTES) >> 4);
-              const uint64_t dk = dk0 + (uint64_t)((s * C::K_BYTES) >> 4);
+              const uint32_t dq = q_lo + static_cast<uint32_t>((t * C::Q_BYTES) >> 4);
+              const uint32_t dk = k_lo + static_cast<uint32_t>((s * C::K_BYTES) >> 4);
 #pragma unroll
               for (int kk = 0; kk < C::QK_STEPS; ++kk) {
                 constexpr int kCh = kBlockQ * C::CHB;  // bytes per 64-element chunk (Q and K tiles alike)
-                const uint64_t off =
-                    (uint64_t)(((kk / C::STEPS_PER_CH) * kCh + (kk % C::STEPS_PER_CH) * C::KSTEP_BYTES) >> 4);
+                const uint32_t off =
+                    static_cast<uint32_t>(((kk / C::STEPS_PER_CH) * kCh + (kk % C::STEPS_PER_CH) * C::KSTEP_BYTES) >> 4);
                 if constexpr (ELEM == kE4M3)
-                  mma_f8_ss(tS, dq + off, dk + off, idesc_qk, kk > 0 ? 1u : 0u);
+                  mma_f8_ss(tS, dq + off, q_hi, dk + off, k_hi, idesc_qk, kk > 0 ? 1u : 0u);
                 else
-                  mma_f16_ss(tS, dq + off, dk + off, idesc_qk, kk > 0 ? 1u : 0u);
+                  mma_f16_ss(tS, dq + off, q_hi, dk + off, k_hi, idesc_qk, kk > 0 ? 1u : 0u);
               }
               mma_commit(&s_full[t]);
               if (j == w.n_t[t] - 1) mma_commit(&q_empty[t]);  // Q_t of this work tile fully used
