@@ -330,25 +330,41 @@ __global__ void __launch_bounds__(kDecodeDv) decode_combine_kernel(const DecodeP
   if (p.lse != nullptr && dv == 0) p.lse[b * p.Hq + h] = ls > 0.f ? (M + __log2f(ls)) * kLn2f : -INFINITY;
 }
 
-// One warp per mask row: for every 128-key block, a 128-bit word with bit c set where
-// mask[b, i, 128 j + c] is -inf, and a flag set where the block row holds any finite
-// non-zero value (those are added to the scores by the prefill kernel from the original
-// mask).  Keys past Sk read as 0.
+// For every (row, 128-key block): a 128-bit word with bit c set where mask[b, i, 128 j + c] is
+// -inf, and a flag set where the block row holds any finite non-zero value (those are added to
+// the scores by the prefill kernel from the original mask).  Keys past Sk read as 0.
+// One warp per (row, group of kMaskGroup blocks): all of the group's loads are issued before
+// the first ballot, so each warp keeps kMaskGroup x 4 coalesced 64-byte reads in flight (mask
+// rows need only 2-byte alignment, which rules out wider loads).
+constexpr int kMaskGroup = 4;
+
 __global__ void __launch_bounds__(128) mask_convert_kernel(const MaskConvertParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * 4 + warp;
-  if (row >= (int64_t)p.B * p.Sq) return;
+  const int n_groups = (p.n_kblocks + kMaskGroup - 1) / kMaskGroup;
+  const int64_t item = (int64_t)blockIdx.x * 4 + warp;
+  if (item >= (int64_t)p.B * p.Sq * n_groups) return;
+  const int64_t row = item / n_groups;
+  const int jb0 = static_cast<int>(item % n_groups) * kMaskGroup;
   const int b = (int)(row / p.Sq), i = (int)(row % p.Sq);
   const uint16_t* src = p.mask + b * p.mask_b + (int64_t)i * p.mask_i;
-  for (int jb = 0; jb < p.n_kblocks; ++jb) {
+  uint16_t v[kMaskGroup][4];
+#pragma unroll
+  for (int g = 0; g < kMaskGroup; ++g)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int col = (jb0 + g) * 128 + q * 32 + lane;
+      v[g][q] = col < p.Sk ? __ldg(src + col) : (uint16_t)0;
+    }
+#pragma unroll
+  for (int g = 0; g < kMaskGroup; ++g) {
+    const int jb = jb0 + g;
+    if (jb >= p.n_kblocks) break;  // the same for the whole warp
     uint32_t wd[4];
     bool general = false;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const int col = jb * 128 + q * 32 + lane;
-      const uint16_t v = col < p.Sk ? src[col] : (uint16_t)0;
-      const bool neg_inf = v == 0xFC00u;
-      general |= !(neg_inf || v == 0u || v == 0x8000u);
+      const bool neg_inf = v[g][q] == 0xFC00u;
+      general |= !(neg_inf || v[g][q] == 0u || v[g][q] == 0x8000u);
       wd[q] = __ballot_sync(0xffffffffu, neg_inf);
     }
     general = __any_sync(0xffffffffu, general);
@@ -382,8 +398,9 @@ cudaError_t launch_decode(int elem, const DecodeParams& p, const CUtensorMap& tk
 }
 
 cudaError_t launch_mask_convert(const MaskConvertParams& p, cudaStream_t st) {
-  const int64_t rows = (int64_t)p.B * p.Sq;
-  mask_convert_kernel<<<(unsigned)((rows + 3) / 4), 128, 0, st>>>(p);
+  const int64_t warps = (int64_t)p.B * p.Sq * ((p.n_kblocks + kMaskGroup - 1) / kMaskGroup);
+  if ((warps + 3) / 4 > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+  mask_convert_kernel<<<(unsigned)((warps + 3) / 4), 128, 0, st>>>(p);
   return cudaGetLastError();
 }
 
