@@ -192,8 +192,9 @@ def prefill_setup(w, dev, rotation=0):
     o = torch.empty((w.B, w.Sq, w.Hq, w.Dv), dtype=out_dtype, device=dev)
     lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
     ws = None
-    if mask is not None:
-        ws = torch.empty(fa.sdpa_fwd_workspace_size(w.B, w.Sq, w.Sk, True), dtype=torch.uint8, device=dev)
+    need = fa.sdpa_fwd_workspace_size(w.B, w.Hq, w.Sq, w.Sk, w.Dv, w.causal, mask is not None)
+    if need > 0:
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
     dq, dk, dv = x["descale"]
 
     def step(_i=0):

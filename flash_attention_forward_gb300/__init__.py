@@ -52,7 +52,7 @@ def _load():
                                f"(or __graft_entry__.build())")
         lib = ctypes.CDLL(LIB_PATH)
         p, i, i64, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
-        lib.sdpa_fwd_workspace_size.argtypes = [i, i, i, i]
+        lib.sdpa_fwd_workspace_size.argtypes = [i, i, i, i, i, i, i]
         lib.sdpa_fwd_workspace_size.restype = sz
         lib.sdpa_fwd.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, p, f, i, p, p, p, sz, i, i, p]
         lib.sdpa_fwd.restype = i
@@ -111,15 +111,17 @@ def _i64(vals):
     return arr
 
 
-def sdpa_fwd_workspace_size(B: int, Sq: int, Sk: int, has_mask: bool) -> int:
-    return int(_load().sdpa_fwd_workspace_size(B, Sq, Sk, int(bool(has_mask))))
+def sdpa_fwd_workspace_size(B: int, Hq: int, Sq: int, Sk: int, Dv: int, causal: bool, has_mask: bool) -> int:
+    """Bytes of prefill workspace for the current device: the condensed mask (required with a
+    mask) followed by the partials of the split last round of work tiles (optional)."""
+    return int(_load().sdpa_fwd_workspace_size(B, Hq, Sq, Sk, Dv, int(bool(causal)), int(bool(has_mask))))
 
 
 def sdpa_decode_workspace_size(B: int, Hq: int, max_kv: int, Dv: int) -> int:
     return int(_load().sdpa_decode_workspace_size(B, Hq, max_kv, Dv))
 
 
-def _fwd_args(q, k, v, out, lse, mask, workspace, out_dtype, return_lse):
+def _fwd_args(q, k, v, out, lse, mask, workspace, out_dtype, return_lse, causal):
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise ValueError("q, k, v must be [B, S, H, D]")
     B, Sq, Hq, D = q.shape
@@ -140,8 +142,9 @@ def _fwd_args(q, k, v, out, lse, mask, workspace, out_dtype, return_lse):
         if mask.dtype != torch.float16 or mask.dim() != 3 or mask.stride(-1) != 1:
             raise ValueError("mask must be an fp16 [B, Sq, Sk] tensor with unit innermost stride")
         mstr = _i64([mask.stride(0), mask.stride(1)])
-        need = sdpa_fwd_workspace_size(B, Sq, Sk, True)
-        if workspace is None:
+    if workspace is None:
+        need = sdpa_fwd_workspace_size(B, Hq, Sq, Sk, Dv, causal, mask is not None)
+        if need > 0:
             workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     return B, Sq, Hq, Hkv, Sk, D, Dv, out, lse, strides, mstr, workspace, ws_bytes
@@ -156,7 +159,7 @@ def sdpa_fwd(q, k, v, *, scale: float | None = None, causal: bool = False, mask=
         raise ValueError("sdpa_fwd takes fp16 or bf16 inputs (use sdpa_fwd_fp8 for e4m3)")
     scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
     B, Sq, Hq, Hkv, Sk, D, Dv, out, lse, strides, mstr, workspace, ws_bytes = _fwd_args(
-        q, k, v, out, lse, mask, workspace, q.dtype, return_lse)
+        q, k, v, out, lse, mask, workspace, q.dtype, return_lse, causal)
     rc = _load().sdpa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk, D, Dv, strides,
                           scale, int(bool(causal)), _ptr(mask), mstr, _ptr(workspace), ws_bytes, _DT[q.dtype],
                           _DT[out.dtype], _stream_ptr(stream))
@@ -172,7 +175,7 @@ def sdpa_fwd_fp8(q, k, v, descale_q: float, descale_k: float, descale_v: float, 
         raise ValueError("sdpa_fwd_fp8 takes float8_e4m3fn inputs")
     scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
     B, Sq, Hq, Hkv, Sk, D, Dv, out, lse, strides, mstr, workspace, ws_bytes = _fwd_args(
-        q, k, v, out, lse, mask, workspace, torch.bfloat16, return_lse)
+        q, k, v, out, lse, mask, workspace, torch.bfloat16, return_lse, causal)
     rc = _load().sdpa_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk, D, Dv, strides,
                               scale, int(bool(causal)), _ptr(mask), mstr, _ptr(workspace), ws_bytes,
                               float(descale_q), float(descale_k), float(descale_v), _DT[out.dtype],

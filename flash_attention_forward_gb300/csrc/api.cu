@@ -88,6 +88,17 @@ size_t mask_ws_bytes(int B, int Sq, int Sk) {
   return round16(rows * nkb * sizeof(uint4)) + round16(rows * nkb);
 }
 
+// Split plan of a prefill launch on the current device (no split if the device query fails).
+SplitPlan fwd_split_plan(int B, int Hq, int Sq, int Sk, bool causal) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();  // clear the error so that later calls do not see it
+    return SplitPlan{};
+  }
+  const long long items = (long long)((Sq + kCtaRows - 1) / kCtaRows) * B * Hq;
+  return prefill_split_plan(items, sms, (Sk + kBlockK - 1) / kBlockK, causal);
+}
+
 int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,
                int Sk, int D, int Dv, const int64_t* strides, float scale, int causal, const void* mask,
                const int64_t* mask_strides, void* workspace, size_t workspace_bytes, int elem, float descale_q,
@@ -128,7 +139,8 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SDPA_ERR_INVALID;
   const int n_kblocks = (Sk + kBlockK - 1) / kBlockK;
   const int n_cta_tiles = (Sq + kCtaRows - 1) / kCtaRows;
-  if ((long long)n_cta_tiles * B * Hq >= (1ll << 31)) return SDPA_ERR_UNSUPPORTED;
+  const long long n_items = (long long)n_cta_tiles * B * Hq;
+  if (n_items * kMaxSplitParts >= (1ll << 31)) return SDPA_ERR_UNSUPPORTED;
   int64_t mb = 0, mi = 0;
   if (mask) {
     if (reinterpret_cast<uintptr_t>(mask) & 1u) return SDPA_ERR_INVALID;
@@ -137,6 +149,13 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
     if (mb < 0 || mi < 0) return SDPA_ERR_INVALID;
     if (!workspace || !aligned16(workspace) || workspace_bytes < mask_ws_bytes(B, Sq, Sk)) return SDPA_ERR_INVALID;
   }
+  // the key-range split of the tail runs only when the caller's workspace also holds its
+  // partial results (sdpa_fwd_workspace_size includes them)
+  const size_t mask_bytes = mask ? mask_ws_bytes(B, Sq, Sk) : 0;
+  SplitPlan sp = fwd_split_plan(B, Hq, Sq, Sk, causal != 0);
+  const size_t split_bytes = prefill_split_bytes(sp, Dv);
+  if (split_bytes == 0 || !workspace || !aligned16(workspace) || workspace_bytes < mask_bytes + split_bytes)
+    sp = SplitPlan{};
 
   // ---- tensor maps
   const CUtensorMapDataType dt = elem == kE4M3   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
@@ -171,6 +190,16 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   p.out_scale = descale_v;
   p.status = status;
   p.stall_first_stage = g_stall_next.exchange(0);
+  p.n_full = (int)(n_items - sp.tail);
+  p.split_tail = sp.tail;
+  p.split_parts = sp.parts;
+  p.n_units = p.n_full + sp.tail * sp.parts;
+  if (sp.parts > 1) {
+    char* base = static_cast<char*>(workspace) + mask_bytes;
+    const size_t rows = (size_t)sp.tail * sp.parts * kCtaRows;
+    p.split_o = reinterpret_cast<float*>(base);
+    p.split_ml = reinterpret_cast<float*>(base + round16(rows * Dv * 4));
+  }
   if (mask) {
     const size_t rows = (size_t)B * (size_t)Sq;
     uint4* bits = static_cast<uint4*>(workspace);
@@ -201,9 +230,10 @@ using namespace sdpa;
 
 extern "C" {
 
-size_t sdpa_fwd_workspace_size(int B, int Sq, int Sk, int has_mask) {
-  if (!has_mask || B < 1 || Sq < 1 || Sk < 1) return 0;
-  return mask_ws_bytes(B, Sq, Sk);
+size_t sdpa_fwd_workspace_size(int B, int Hq, int Sq, int Sk, int Dv, int causal, int has_mask) {
+  if (B < 1 || Hq < 1 || Sq < 1 || Sk < 1 || Dv < 1) return 0;
+  const size_t mask_bytes = has_mask ? mask_ws_bytes(B, Sq, Sk) : 0;
+  return mask_bytes + prefill_split_bytes(fwd_split_plan(B, Hq, Sq, Sk, causal != 0), Dv);
 }
 
 int sdpa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,

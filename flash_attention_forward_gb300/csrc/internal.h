@@ -41,7 +41,43 @@ struct PrefillParams {
   int64_t mask_b, mask_i;  // element strides of the original mask
   uint32_t* status;        // device status word
   int stall_first_stage;   // test hook: the producer never fills the first K/V stage
+  // Work units: n_full whole work tiles, then split_tail work tiles cut into split_parts key
+  // ranges each (see prefill_split_plan); n_units = n_full + split_tail * split_parts.
+  int n_units, n_full, split_tail, split_parts;
+  float* split_o;          // [split_tail, split_parts, kCtaRows, DV] unnormalised fp32 O
+  float* split_ml;         // [split_tail, split_parts, kCtaRows, 2] row max (log2 units), row sum
 };
+
+// Key-range split of the last, partial wave of work tiles.  With items work tiles on sms
+// persistent CTAs, items % sms tiles are left for a final round that would keep most SMs idle;
+// when the attention is not causal (all tiles equally long) each of those tail tiles is cut
+// into `parts` key ranges that run on otherwise idle SMs; a combine kernel then merges the
+// parts' (O, max, sum) of every row with log-sum-exp weights.
+constexpr int kMaxSplitParts = 8;
+struct SplitPlan {
+  int tail = 0;   // work tiles split (the last `tail` in launch order)
+  int parts = 1;  // key ranges per split tile (1 = no split)
+};
+inline SplitPlan prefill_split_plan(long long items, int sms, int n_kblocks, bool causal) {
+  SplitPlan sp;
+  if (causal || sms < 2 || items <= 0) return sp;
+  const long long tail = items % sms;
+  if (tail == 0) return sp;
+  long long parts = sms / tail;
+  if (parts > kMaxSplitParts) parts = kMaxSplitParts;
+  if (parts > n_kblocks) parts = n_kblocks;
+  if (parts < 2) return sp;
+  sp.tail = static_cast<int>(tail);
+  sp.parts = static_cast<int>(parts);
+  return sp;
+}
+inline size_t split_round16(size_t x) { return (x + 15) & ~size_t(15); }
+// Workspace bytes of a split plan: partial O, then partial (max, sum).
+inline size_t prefill_split_bytes(const SplitPlan& sp, int Dv) {
+  if (sp.parts < 2) return 0;
+  const size_t rows = static_cast<size_t>(sp.tail) * sp.parts * kCtaRows;
+  return split_round16(rows * Dv * 4) + split_round16(rows * 2 * 4);
+}
 
 struct DecodeParams {
   const void* q;

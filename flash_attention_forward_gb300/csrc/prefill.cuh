@@ -119,11 +119,15 @@ __device__ __forceinline__ uint4 e4m3x8_to_f16x8(uint2 in) {
   return out;
 }
 
-// One work tile: two consecutive 128-row query tiles of one (batch, query head).
+// One work unit: two consecutive 128-row query tiles of one (batch, query head) against the
+// key blocks [jb0, jb0 + n_blocks), which is every block the tiles need unless the work tile is
+// split (split >= 0: part `part` of p.split_parts key ranges of split work tile `split`).
 struct WorkTile {
   int b, h, kvh, q0;
   int n_t[kTilesPerCta];  // K/V blocks each query tile needs (0 = tile entirely past Sq)
-  int n_blocks;           // blocks streamed for the work tile = max over its query tiles
+  int n_blocks;           // blocks streamed for the unit = max over its query tiles
+  int jb0;                // first key block
+  int split, part;        // split work tile and key range, or split = -1
 };
 
 // Work tiles in launch order.  A KV unit is one (batch, KV head): its K/V are shared by the
@@ -133,8 +137,21 @@ struct WorkTile {
 // Inside a group, causal tiles at the bottom of the matrix see the most keys and come first;
 // tiles of one row band are ordered by unit, then query head.
 template <bool CAUSAL>
-__device__ __forceinline__ WorkTile work_tile(const PrefillParams& p, int item) {
+__device__ __forceinline__ WorkTile work_tile(const PrefillParams& p, int work_unit) {
   WorkTile w;
+  // work units past the whole work tiles are key ranges of the split tail (never causal)
+  int item = work_unit, parts = 1;
+  w.split = -1, w.part = 0;
+  if (!CAUSAL && work_unit >= p.n_full) {
+    const int r = work_unit - p.n_full;
+    parts = p.split_parts;
+    w.split = r / parts;
+    w.part = r - w.split * parts;
+    item = p.n_full + w.split;
+  }
+  const int jb0 = w.part * p.n_kblocks / parts;
+  const int jb1 = (w.part + 1) * p.n_kblocks / parts;
+  w.jb0 = jb0;
   const int G = p.group;                           // query heads per KV head
   const int units = p.B * p.Hkv;
   const int per_unit = G * p.n_cta_tiles;          // work tiles of one KV unit
@@ -157,7 +174,7 @@ __device__ __forceinline__ WorkTile work_tile(const PrefillParams& p, int item) 
     const int r0 = w.q0 + t * kBlockQ;
     int n = 0;
     if (r0 < p.Sq) {
-      n = p.n_kblocks;
+      n = jb1 - jb0;
       if (CAUSAL) {
         const int last_row = min(r0 + kBlockQ - 1, p.Sq - 1);
         n = min(n, last_row / kBlockK + 1);
@@ -169,7 +186,7 @@ __device__ __forceinline__ WorkTile work_tile(const PrefillParams& p, int item) 
   return w;
 }
 
-// The k-th work tile of CTA c (snake order over the longest-first list: forward on even
+// The k-th work unit of CTA c (snake order over the longest-first list: forward on even
 // rounds, backward on odd ones, which evens out the per-CTA totals of a causal schedule).
 __device__ __forceinline__ int nth_item(int k) {
   const int G = gridDim.x;
@@ -225,7 +242,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int n_items = p.n_cta_tiles * p.B * p.Hq;
+  const int n_items = p.n_units;
 
   if (tid == 0) {
     for (int t = 0; t < 2; ++t) {
@@ -292,39 +309,34 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             mbar_arrive_expect_tx(&in_full[s], C::K_BYTES);
             for (int c = 0; c < C::NCH_D; ++c)
               tma_load_4d(sK + s * C::K_BYTES + c * kBlockK * C::CHB, &tm_k, &in_full[s], c * C::CH, w.kvh,
-                          j * kBlockK, w.b);
+                          (w.jb0 + j) * kBlockK, w.b);
             if (r > 0 && !mbar_wait(&v_free[s], (r - 1) & 1, abort_flag, p.status)) {
               ok = false;
               break;
             }
             mbar_arrive_expect_tx(&v_full[s], C::VRAW_BYTES);
-            tma_load_4d(sVraw + s * C::VRAW_BYTES, &tm_v, &v_full[s], 0, w.kvh, j * kBlockK, w.b);
+            tma_load_4d(sVraw + s * C::VRAW_BYTES, &tm_v, &v_full[s], 0, w.kvh, (w.jb0 + j) * kBlockK, w.b);
           }
-          continue;
-        }
-        // step j of the work tile brings K(j) and V(j-1)
-        for (int j = 0; ok && j <= w.n_blocks; ++j, ++g) {
-          const int s = g % ST, r = g / ST;
-          const bool has_k = j < w.n_blocks, has_v = j >= 1;
-          if (r > 0 && !mbar_wait(&released[s], (r - 1) & 1, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          if (p.stall_first_stage && g == 0) continue;  // test hook: stage 0 never fills
-          constexpr uint32_t v_bytes = (ELEM == kE4M3) ? C::VRAW_BYTES : C::V_BYTES;
-          mbar_arrive_expect_tx(&in_full[s], (has_k ? C::K_BYTES : 0) + (has_v ? v_bytes : 0));
-          if (has_k) {
-            for (int c = 0; c < C::NCH_D; ++c)
-              tma_load_4d(sK + s * C::K_BYTES + c * kBlockK * C::CHB, &tm_k, &in_full[s], c * C::CH, w.kvh,
-                          j * kBlockK, w.b);
-          }
-          if (has_v) {
-            if constexpr (ELEM == kE4M3) {
-              tma_load_4d(sVraw + s * C::VRAW_BYTES, &tm_v, &in_full[s], 0, w.kvh, (j - 1) * kBlockK, w.b);
-            } else {
+        } else {
+          // step j of the work tile brings K(j) and V(j-1)
+          for (int j = 0; ok && j <= w.n_blocks; ++j, ++g) {
+            const int s = g % ST, r = g / ST;
+            const bool has_k = j < w.n_blocks, has_v = j >= 1;
+            if (r > 0 && !mbar_wait(&released[s], (r - 1) & 1, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            if (p.stall_first_stage && g == 0) continue;  // test hook: stage 0 never fills
+            mbar_arrive_expect_tx(&in_full[s], (has_k ? C::K_BYTES : 0) + (has_v ? C::V_BYTES : 0));
+            if (has_k) {
+              for (int c = 0; c < C::NCH_D; ++c)
+                tma_load_4d(sK + s * C::K_BYTES + c * kBlockK * C::CHB, &tm_k, &in_full[s], c * C::CH, w.kvh,
+                            (w.jb0 + j) * kBlockK, w.b);
+            }
+            if (has_v) {
               for (int c = 0; c < C::NCH_V; ++c)
                 tma_load_4d(sV + s * C::V_BYTES + c * kBlockK * 128, &tm_v, &in_full[s], c * 64, w.kvh,
-                            (j - 1) * kBlockK, w.b);
+                            (w.jb0 + j - 1) * kBlockK, w.b);
             }
           }
         }
@@ -516,8 +528,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         uint32_t mflag = 0;
         if constexpr (MASK) {
           if (row_valid) {
-            mbits = __ldg(bits_row + j);
-            mflag = __ldg(flags_row + j);
+            mbits = __ldg(bits_row + w.jb0 + j);
+            mflag = __ldg(flags_row + w.jb0 + j);
           }
         }
         if (!mbar_wait_warp(&s_full[t], sn & 1, abort_flag, p.status)) {
@@ -546,7 +558,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           }
         }
         // the causal diagonal and the ragged last block: hide keys past the row / past Sk
-        const int k0 = j * kBlockK;
+        const int k0 = (w.jb0 + j) * kBlockK;
         const bool edge = (CAUSAL && (k0 + kBlockK - 1 > w.q0 + t * kBlockQ)) || (k0 + kBlockK > p.Sk);
         if (edge) {
           const int lim = (CAUSAL ? min(p.Sk, qrow + 1) : p.Sk) - k0;
@@ -644,10 +656,35 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       }
       ++on;
       tc_fence_after();
-      const float inv = (l > 0.f) ? p.out_scale / l : 0.f;
       uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
                       2 * (static_cast<int64_t>(w.b) * p.o_b + static_cast<int64_t>(qrow) * p.o_s +
                            static_cast<int64_t>(w.h) * p.o_h);
+      float* lse_out = p.lse ? p.lse + (static_cast<int64_t>(w.b) * p.Hq + w.h) * p.Sq + qrow : nullptr;
+      if (w.split >= 0) {
+        // one key range of a split work tile: store this part's unnormalised O row, row max
+        // and row sum for split_combine_kernel
+        const int prow = t * kBlockQ + row;
+        const size_t slot = (static_cast<size_t>(w.split) * p.split_parts + w.part) * kCtaRows + prow;
+        float* po = p.split_o + slot * DV;
+#pragma unroll 1
+        for (int c = 0; c < DV / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_ld_wait();
+          reg_fence(o);
+          if (row_valid) {
+            uint4* dst = reinterpret_cast<uint4*>(po + c * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+          }
+          __syncwarp();
+        }
+        tc_fence_before();
+        mbar_arrive(&o_empty[t]);
+        if (row_valid) *reinterpret_cast<float2*>(p.split_ml + slot * 2) = make_float2(m_used, l);
+        continue;
+      }
+      const float inv = (l > 0.f) ? p.out_scale / l : 0.f;
 #pragma unroll 1
       for (int c = 0; c < DV / 32; ++c) {
         uint32_t o[32];
@@ -668,9 +705,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       // O_t has been read: the next work tile's first P.V may overwrite it
       tc_fence_before();
       mbar_arrive(&o_empty[t]);
-      if (p.lse != nullptr && row_valid)
-        p.lse[(static_cast<int64_t>(w.b) * p.Hq + w.h) * p.Sq + qrow] =
-            (l > 0.f) ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+      if (lse_out != nullptr && row_valid) *lse_out = (l > 0.f) ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
     }
   }
 
@@ -681,6 +716,60 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, 512);
   }
+}
+
+// Merges the split_parts partial results of every row of the split work tiles and writes the
+// normalised O and LSE (runs after prefill_kernel in the same stream).  One thread per (split
+// tile, row, 8 output columns):
+//   M = max_q m_q,  w_q = 2^(m_q - M),  O = sum_q w_q O_q / sum_q w_q l_q,  LSE = (M + log2 L) ln 2,
+// parts taken in order, so the result does not depend on which part finished first.
+template <int ELEM, int DV>
+__global__ void __launch_bounds__(128) split_combine_kernel(const PrefillParams p) {
+  constexpr int kChunks = DV / 8;
+  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<long long>(p.split_tail) * kCtaRows * kChunks) return;
+  const int chunk = static_cast<int>(idx % kChunks);
+  const int prow = static_cast<int>((idx / kChunks) % kCtaRows);
+  const int split = static_cast<int>(idx / (static_cast<long long>(kChunks) * kCtaRows));
+  const int P = p.split_parts;
+  const WorkTile w = work_tile<false>(p, p.n_full + split * P);
+  const int qrow = w.q0 + prow;
+  if (qrow >= p.Sq) return;
+  const size_t slot0 = static_cast<size_t>(split) * P * kCtaRows + prow;
+  float m[kMaxSplitParts], l[kMaxSplitParts];
+  float M = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < kMaxSplitParts; ++q) {
+    if (q < P) {
+      const float2 ml = *reinterpret_cast<const float2*>(p.split_ml + (slot0 + static_cast<size_t>(q) * kCtaRows) * 2);
+      m[q] = ml.x, l[q] = ml.y;
+    } else {
+      m[q] = -INFINITY, l[q] = 0.f;
+    }
+    M = fmaxf(M, m[q]);
+  }
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float L = 0.f;
+#pragma unroll
+  for (int q = 0; q < kMaxSplitParts; ++q) {
+    if (q < P) {
+      const float wq = (m[q] == -INFINITY) ? 0.f : ex2(m[q] - M);
+      L += wq * l[q];
+      const float4* src = reinterpret_cast<const float4*>(p.split_o + (slot0 + static_cast<size_t>(q) * kCtaRows) * DV) + 2 * chunk;
+      const float4 a = src[0], b = src[1];
+      acc[0] += wq * a.x, acc[1] += wq * a.y, acc[2] += wq * a.z, acc[3] += wq * a.w;
+      acc[4] += wq * b.x, acc[5] += wq * b.y, acc[6] += wq * b.z, acc[7] += wq * b.w;
+    }
+  }
+  const float inv = (L > 0.f) ? p.out_scale / L : 0.f;
+  uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
+                  2 * (static_cast<int64_t>(w.b) * p.o_b + static_cast<int64_t>(qrow) * p.o_s +
+                       static_cast<int64_t>(w.h) * p.o_h);
+  *reinterpret_cast<uint4*>(orow + chunk * 16) =
+      make_uint4(pack_out<ELEM>(acc[0] * inv, acc[1] * inv), pack_out<ELEM>(acc[2] * inv, acc[3] * inv),
+                 pack_out<ELEM>(acc[4] * inv, acc[5] * inv), pack_out<ELEM>(acc[6] * inv, acc[7] * inv));
+  if (chunk == 0 && p.lse != nullptr)
+    p.lse[(static_cast<int64_t>(w.b) * p.Hq + w.h) * p.Sq + qrow] = (L > 0.f) ? (M + __log2f(L)) * kLn2 : -INFINITY;
 }
 
 }  // namespace sdpa

@@ -13,12 +13,12 @@ cudaError_t launch_prefill_instance(const CUtensorMap& tq, const CUtensorMap& tk
   // the shared-memory opt-in is per device; setting it again is harmless
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  // persistent: one CTA per SM (shared memory admits no second one), looping over work tiles
+  // persistent: one CTA per SM (shared memory admits no second one), looping over work units
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  const long long items = (long long)p.n_cta_tiles * p.B * p.Hq;
-  const unsigned grid = (unsigned)(items < sms ? items : sms);
+  const long long units = p.n_units;
+  const unsigned grid = (unsigned)(units < sms ? units : sms);
   // Group KV units so that a group is a whole number of snake round pairs (2 x grid work
   // tiles; the snake balances inside it) and its K/V stays within a 64 MiB share of L2.
   PrefillParams q = p;
@@ -30,9 +30,14 @@ cudaError_t launch_prefill_instance(const CUtensorMap& tq, const CUtensorMap& tk
   const long long kv_unit_bytes = (long long)p.Sk * (D * C::ESZ + DV * C::ESZ);
   const long long cap = (64LL << 20) / (kv_unit_bytes > 0 ? kv_unit_bytes : 1);
   long long ug = aligned < cap ? aligned : cap;
-  const long long units = (long long)p.B * p.Hkv;
-  q.units_per_group = (int)(ug < 1 ? 1 : (ug > units ? units : ug));
+  const long long kv_units = (long long)p.B * p.Hkv;
+  q.units_per_group = (int)(ug < 1 ? 1 : (ug > kv_units ? kv_units : ug));
   kern<<<grid, kPrefillThreads, C::SMEM, st>>>(tq, tk, tv, q);
+  if (!CAUSAL && p.split_parts > 1) {
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const long long threads = (long long)p.split_tail * kCtaRows * (DV / 8);
+    split_combine_kernel<ELEM == kE4M3 ? kBF16 : ELEM, DV><<<(unsigned)((threads + 127) / 128), 128, 0, st>>>(q);
+  }
   return cudaGetLastError();
 }
 

@@ -57,12 +57,19 @@ typedef enum { SDPA_F16 = 0, SDPA_BF16 = 1, SDPA_E4M3 = 2 } sdpa_dtype;
 #define SDPA_DECODE_NSTRIDES 10
 
 /*
- * sdpa_fwd_workspace_size -- bytes of device scratch sdpa_fwd / sdpa_fwd_fp8 need.
- * Zero when has_mask == 0.  With an additive mask the library first condenses it into
- * one bit per (row, key) marking -inf entries plus one flag per (row, 128-key block)
- * marking blocks that hold finite non-zero values; this is that buffer.
+ * sdpa_fwd_workspace_size -- bytes of device scratch sdpa_fwd / sdpa_fwd_fp8 use, for the
+ * current device (the SM count enters the second part).  Two parts, in this order:
+ *  1. with an additive mask (has_mask != 0): the mask condensed into one bit per (row, key)
+ *     marking -inf entries plus one flag per (row, 128-key block) marking blocks that hold
+ *     finite non-zero values.  Required: a masked call with less workspace is rejected.
+ *  2. without causal masking, when the work tiles of 2 x 128 query rows do not divide evenly
+ *     over the SMs: partial results of the last, partial round of tiles, whose key range is
+ *     split over the otherwise idle SMs (unnormalised fp32 O, row max and row sum per part);
+ *     a second kernel in the same stream merges them with log-sum-exp weights.  Optional:
+ *     with less workspace the call runs unsplit; results agree within rounding.
+ * Zero when neither applies.  Sizes below 1 give 0.
  */
-size_t sdpa_fwd_workspace_size(int B, int Sq, int Sk, int has_mask);
+size_t sdpa_fwd_workspace_size(int B, int Hq, int Sq, int Sk, int Dv, int causal, int has_mask);
 
 /*
  * sdpa_fwd -- fused attention prefill, fp16 or bf16 inputs, fp32 softmax state.
@@ -78,8 +85,11 @@ size_t sdpa_fwd_workspace_size(int B, int Sq, int Sk, int has_mask);
  *            after scaling; element strides mask_strides = {m_b, m_i} (NULL means
  *            {Sq*Sk, Sk}; m_b may be 0 to broadcast over the batch).  Only 2-byte
  *            alignment is required.
- *   workspace: device scratch of at least sdpa_fwd_workspace_size(B, Sq, Sk, mask!=0)
- *            bytes, 16-byte aligned; may be NULL when mask is NULL.
+ *   workspace: device scratch, 16-byte aligned, contents on entry irrelevant: at least the
+ *            mask part of sdpa_fwd_workspace_size(B, Hq, Sq, Sk, Dv, causal, mask!=0) when
+ *            mask != NULL; the full size enables the split of the last round of tiles.
+ *            May be NULL when mask is NULL.  Calls that overlap on the GPU need separate
+ *            workspaces.
  *   in_dtype: SDPA_F16 or SDPA_BF16.  out_dtype: SDPA_F16 or SDPA_BF16.
  *
  * Supported head dims: (D, Dv) in {(64, 64), (128, 128)}.  q/k/v/o base pointers must be

@@ -30,10 +30,12 @@ def test_status_strings_and_version(lib):
 
 
 def test_workspace_sizes(lib):
-    assert fa.sdpa_fwd_workspace_size(3, 1000, 3001, False) == 0
-    n = fa.sdpa_fwd_workspace_size(3, 1000, 3001, True)
+    # no GPU here: the device-dependent split part is zero, only the condensed mask remains
+    assert fa.sdpa_fwd_workspace_size(3, 28, 1000, 3001, 128, False, False) == 0
+    n = fa.sdpa_fwd_workspace_size(3, 28, 1000, 3001, 128, False, True)
     rows, nkb = 3 * 1000, (3001 + 127) // 128
     assert n >= rows * nkb * 17 and n % 16 == 0
+    assert fa.sdpa_fwd_workspace_size(0, 28, 1000, 3001, 128, False, True) == 0
     d = fa.sdpa_decode_workspace_size(64, 32, 16384, 128)
     assert d == 64 * 32 * 16 * 130 * 4
     assert fa.sdpa_decode_workspace_size(0, 32, 16384, 128) == 0

@@ -55,6 +55,49 @@ def test_small_shapes_match_oracle(shape, dtype, causal, use_mask):
     assert_lse_close(lse.cpu().numpy(), ref_lse, TOL_LSE_F16 if dtype == "f16" else TOL_LSE_BF16)
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_split_tail_agrees_with_unsplit_and_oracle(dtype):
+    # 6 work tiles of 2 x 128 rows are far fewer than the SMs: each is split into 8 key ranges
+    # (when the workspace holds the partials) and merged; with a workspace too small for the
+    # partials the same call runs unsplit.  Both must match the oracle.
+    B, Hq, Hkv, Sq, Sk, D = 1, 3, 1, 500, 2000, 128
+    x = workloads.custom_prefill(B, Hq, Hkv, Sq, Sk, D, D, dtype=dtype, seed=913)
+    scale = 1.0 / np.sqrt(D)
+    q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
+    need = fa.sdpa_fwd_workspace_size(B, Hq, Sq, Sk, D, False, False)
+    assert need > 0
+    o_split, lse_split = fa.sdpa_fwd(q, k, v, scale=scale, workspace=torch.empty(need, dtype=torch.uint8, device=DEV))
+    o_whole, lse_whole = fa.sdpa_fwd(q, k, v, scale=scale, workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
+    torch.cuda.synchronize()
+    assert fa.sdpa_check_device_status() == fa.SDPA_OK
+    ref_o, ref_lse = oracle.sdpa_fwd(x["q"], x["k"], x["v"], scale=scale)
+    tol_lse = TOL_LSE_F16 if dtype == "f16" else TOL_LSE_BF16
+    for o, lse in ((o_split, lse_split), (o_whole, lse_whole)):
+        assert_close(o.float().cpu().numpy(), ref_o, TOL_16BIT)
+        assert_lse_close(lse.cpu().numpy(), ref_lse, tol_lse)
+    # the causal path never splits: its workspace size is zero without a mask
+    assert fa.sdpa_fwd_workspace_size(B, Hq, Sq, Sk, D, True, False) == 0
+
+
+def test_split_with_key_ranges_fully_masked_for_some_rows():
+    # rows whose visible keys fall in only some of the split key ranges: the other ranges
+    # contribute max = -inf and sum = 0 to the merge; fully masked rows give O = 0, LSE = -inf
+    B, Hq, Hkv, Sq, Sk, D = 1, 2, 2, 300, 1500, 64
+    x = workloads.custom_prefill(B, Hq, Hkv, Sq, Sk, D, D, dtype="bf16", seed=57)
+    mask = torch.zeros((B, Sq, Sk), dtype=torch.float16)
+    mask[:, 0:100, :1000] = float("-inf")      # only the last ranges are visible
+    mask[:, 100:150, 200:] = float("-inf")     # only the first ranges are visible
+    mask[:, 150:160, :] = float("-inf")        # nothing visible
+    mask[:, 160:170, 700:701] = 3.0            # a finite non-zero value inside one range
+    x["mask"] = mask
+    scale = 1.0 / np.sqrt(D)
+    o, lse = _run(x, scale, False, True)
+    ref_o, ref_lse = oracle.sdpa_fwd(x["q"], x["k"], x["v"], x["mask"], scale=scale)
+    assert_close(o.float().cpu().numpy(), ref_o, TOL_16BIT)
+    assert_lse_close(lse.cpu().numpy(), ref_lse, TOL_LSE_BF16)
+    assert torch.all(o[:, 150:160] == 0) and torch.all(torch.isneginf(lse[:, :, 150:160]))
+
+
 def test_tiny_workload_full_output():
     w = workloads.WORKLOADS["tiny_prefill_f16_d64"]
     x = workloads.prefill_inputs(w)
