@@ -112,11 +112,11 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
         std::isfinite(descale_v) && descale_v > 0.f))
     return SDPA_ERR_INVALID;
   const int esize = (elem == kE4M3) ? 1 : 2;
+  // head dims built for every input type: (64, 64), (128, 128), (192, 128)
+  if (!((D == 64 && Dv == 64) || (D == 128 && Dv == 128) || (D == 192 && Dv == 128))) return SDPA_ERR_UNSUPPORTED;
   if (elem == kE4M3) {
-    if (!((D == 128 && Dv == 128) || (D == 192 && Dv == 128))) return SDPA_ERR_UNSUPPORTED;
     if (out_dtype != SDPA_BF16) return SDPA_ERR_UNSUPPORTED;
   } else {
-    if (!((D == 64 && Dv == 64) || (D == 128 && Dv == 128))) return SDPA_ERR_UNSUPPORTED;
     if ((elem == kF16 && out_dtype != SDPA_F16) || (elem == kBF16 && out_dtype != SDPA_BF16))
       return SDPA_ERR_UNSUPPORTED;
   }

@@ -42,7 +42,9 @@ struct PrefillCfg {
   static constexpr uint32_t SW = (CHB == 128) ? kSwizzle128B : kSwizzle64B;
   static constexpr int NCH_D = D / CH;
   static constexpr int NCH_V = DV / 64;         // V is always 16-bit in shared memory
-  static constexpr int STAGES = (D <= 64) ? 4 : 2;
+  // ring depth: 4 stages for D = 64, 2 otherwise; 16-bit D = 192 has room for one stage only
+  // (two Q tiles of 48 KB plus one K + V stage of 80 KB), so its loads and MMAs take turns
+  static constexpr int STAGES = (D <= 64) ? 4 : (ESZ == 2 && D > 128) ? 1 : 2;
   static constexpr int Q_BYTES = kBlockQ * D * ESZ;
   static constexpr int K_BYTES = kBlockK * D * ESZ;
   static constexpr int V_BYTES = kBlockK * DV * 2;

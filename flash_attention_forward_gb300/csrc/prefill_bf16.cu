@@ -1,4 +1,4 @@
-// Prefill instances for bf16 inputs: (D, Dv) in {(64, 64), (128, 128)} x causal x mask.
+// Prefill instances for bf16 inputs: (D, Dv) in {(64, 64), (128, 128), (192, 128)} x causal x mask.
 #include "prefill_launch.cuh"
 
 namespace sdpa {
@@ -9,6 +9,7 @@ cudaError_t launch_prefill_bf16(int D, int Dv, bool causal, bool has_mask, const
   *supported = true;
   if (D == 64 && Dv == 64) return launch_prefill_dims<kBF16, 64, 64>(causal, has_mask, tq, tk, tv, p, st);
   if (D == 128 && Dv == 128) return launch_prefill_dims<kBF16, 128, 128>(causal, has_mask, tq, tk, tv, p, st);
+  if (D == 192 && Dv == 128) return launch_prefill_dims<kBF16, 192, 128>(causal, has_mask, tq, tk, tv, p, st);
   *supported = false;
   return cudaSuccess;
 }

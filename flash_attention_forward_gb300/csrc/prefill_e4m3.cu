@@ -1,4 +1,4 @@
-// Prefill instances for e4m3 inputs: (D, Dv) in {(128, 128), (192, 128)} x causal x mask.
+// Prefill instances for e4m3 inputs: (D, Dv) in {(64, 64), (128, 128), (192, 128)} x causal x mask.
 #include "prefill_launch.cuh"
 
 namespace sdpa {
@@ -7,6 +7,7 @@ cudaError_t launch_prefill_e4m3(int D, int Dv, bool causal, bool has_mask, const
                                 const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st,
                                 bool* supported) {
   *supported = true;
+  if (D == 64 && Dv == 64) return launch_prefill_dims<kE4M3, 64, 64>(causal, has_mask, tq, tk, tv, p, st);
   if (D == 128 && Dv == 128) return launch_prefill_dims<kE4M3, 128, 128>(causal, has_mask, tq, tk, tv, p, st);
   if (D == 192 && Dv == 128) return launch_prefill_dims<kE4M3, 192, 128>(causal, has_mask, tq, tk, tv, p, st);
   *supported = false;

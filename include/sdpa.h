@@ -92,7 +92,8 @@ size_t sdpa_fwd_workspace_size(int B, int Hq, int Sq, int Sk, int Dv, int causal
  *            workspaces.
  *   in_dtype: SDPA_F16 or SDPA_BF16.  out_dtype: SDPA_F16 or SDPA_BF16.
  *
- * Supported head dims: (D, Dv) in {(64, 64), (128, 128)}.  q/k/v/o base pointers must be
+ * Supported head dims: (D, Dv) in {(64, 64), (128, 128), (192, 128)} (D = 192 keeps one K/V stage
+ * in shared memory next to two 48 KB Q tiles, so its loads do not overlap its MMAs).  q/k/v/o base pointers must be
  * 16-byte aligned and their s/h/b strides multiples of 8 elements (tensor-memory-access
  * descriptor rule); otherwise SDPA_ERR_UNSUPPORTED.  Sizes: B, Hq, Hkv, Sq, Sk >= 1.
  */
@@ -109,7 +110,7 @@ int sdpa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
  * multiplied by descale_v in the epilogue.  (page "MlaMmaOp", struct summary: the
  * MLA prefill path streams FP8 e4m3 K/V with D != Dv.)
  *
- * Supported head dims: (D, Dv) in {(128, 128), (192, 128)}.  q/k/v strides must be
+ * Supported head dims: (D, Dv) in {(64, 64), (128, 128), (192, 128)}.  q/k/v strides must be
  * multiples of 16 elements.  out_dtype: SDPA_BF16 or SDPA_F16.  Other arguments as in
  * sdpa_fwd.
  */

@@ -37,6 +37,18 @@ def test_small_shapes_match_oracle(shape, D, causal):
     assert_lse_close(lse.cpu().numpy(), ref_lse, TOL_LSE_F16)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", [(1, 2, 1, 129, 200), (2, 4, 4, 300, 300)])
+def test_d64_matches_oracle(shape, causal):
+    B, Hq, Hkv, Sq, Sk = shape
+    x = workloads.custom_prefill(B, Hq, Hkv, Sq, Sk, 64, 64, dtype="e4m3", seed=Sq + Sk + causal + 64)
+    o, lse = _run(x, 0.125, causal)
+    assert o.shape[-1] == 64
+    ref_o, ref_lse = oracle.sdpa_fwd(x["q"], x["k"], x["v"], scale=0.125, causal=causal, descale=x["descale"])
+    assert_close(o.float().cpu().numpy(), ref_o, TOL_FP8)
+    assert_lse_close(lse.cpu().numpy(), ref_lse, TOL_LSE_F16)
+
+
 def test_fp8_with_mask():
     x = workloads.custom_prefill(2, 2, 2, 300, 500, 192, 128, dtype="e4m3", seed=41, mask=True)
     o, lse = _run(x, 1 / np.sqrt(192), True, use_mask=True)

@@ -56,6 +56,24 @@ def test_small_shapes_match_oracle(shape, dtype, causal, use_mask):
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("use_mask", [False, True])
+@pytest.mark.parametrize("shape", [(1, 2, 1, 300, 500), (2, 4, 2, 257, 129), (1, 1, 1, 1, 1)])
+def test_d192_dv128_matches_oracle(shape, dtype, causal, use_mask):
+    # Dv != D on 16-bit inputs: the QK contraction runs over 192 dims, P.V produces 128
+    B, Hq, Hkv, Sq, Sk = shape
+    x = workloads.custom_prefill(B, Hq, Hkv, Sq, Sk, 192, 128, dtype=dtype, seed=Sq * 7 + Sk + causal + 2 * use_mask,
+                                 mask=use_mask, masked_frac=0.1, full_row_frac=0.05)
+    scale = 1.0 / np.sqrt(192)
+    o, lse = _run(x, scale, causal, use_mask)
+    assert o.shape[-1] == 128
+    ref_o, ref_lse = oracle.sdpa_fwd(x["q"], x["k"], x["v"], x["mask"] if use_mask else None, scale=scale,
+                                     causal=causal)
+    assert_close(o.float().cpu().numpy(), ref_o, TOL_16BIT)
+    assert_lse_close(lse.cpu().numpy(), ref_lse, TOL_LSE_F16 if dtype == "f16" else TOL_LSE_BF16)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
 def test_split_tail_agrees_with_unsplit_and_oracle(dtype):
     # 6 work tiles of 2 x 128 rows are far fewer than the SMs: each is split into 8 key ranges
     # (when the workspace holds the partials) and merged; with a workspace too small for the
