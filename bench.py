@@ -232,7 +232,9 @@ def bench_prefill(w, K, W, dev, peaks, flusher):
     return r
 
 
-def bench_decode(w, K, W, dev, peaks):
+def bench_decode(w, K, W, dev, peaks, page_size: int = 64):
+    """The split-KV decode over 4 rotating input sets (each far larger than L2), then the same
+    rows in page_size-row pages scattered over a pool (the paged decode).  Returns both lines."""
     import flash_attention_forward_gb300 as fa
 
     sets = []
@@ -245,21 +247,38 @@ def bench_decode(w, K, W, dev, peaks):
     o = torch.empty((w.B, w.Hq, w.Dv), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
     ws = torch.empty(fa.sdpa_decode_workspace_size(w.B, w.Hq, w.Sk, w.Dv), dtype=torch.uint8, device=dev)
+    hbm = peaks["hbm_gbs"]
+
+    def line(name, ms, launches, extra=None):
+        by = [sets[i % 4]["bytes"] for i in range(K)]
+        gbs = [b / (t * 1e-3) / 1e9 for b, t in zip(by, ms)]
+        value = sum(by) / (sum(ms) * 1e-3) / 1e9
+        r = {"workload": name, "value": value, "unit": "GB/s", "ms_per_step": sum(ms) / K, "bytes_per_step": sum(by) / K,
+             "launches_per_step": launches, "per_step_gbs_min": min(gbs),
+             "roofline": {"bound": "hbm", "achieved": value, "peak": hbm, "unit": "GB/s", "frac": value / hbm,
+                          "peak_note": "copy bandwidth, of " + peaks["source"], "traffic": recorded_traffic(name)}}
+        if extra:
+            r.update(extra)
+        return r
 
     def step(i):
         s = sets[i % 4] if i >= 0 else sets[0]
         fa.sdpa_decode(s["q"], s["k"], s["v"], s["kv_len"], scale=w.scale, out=o, lse=lse, workspace=ws)
 
-    ms = time_steps(step, K, W)
-    by = [sets[i % 4]["bytes"] for i in range(K)]
-    gbs = [b / (t * 1e-3) / 1e9 for b, t in zip(by, ms)]
-    avg_ms = sum(ms) / K
-    value = sum(by) / (sum(ms) * 1e-3) / 1e9
-    hbm = peaks["hbm_gbs"]
-    return {"workload": w.name, "value": value, "unit": "GB/s", "ms_per_step": avg_ms, "bytes_per_step": sum(by) / K,
-            "launches_per_step": 2, "per_step_gbs_min": min(gbs),
-            "roofline": {"bound": "hbm", "achieved": value, "peak": hbm, "unit": "GB/s", "frac": value / hbm,
-                         "peak_note": "copy bandwidth, of " + peaks["source"], "traffic": recorded_traffic(w.name)}}
+    contiguous = line(w.name, time_steps(step, K, W), 2)
+    for r, d in enumerate(sets):  # the same rows, paged: every page lands at a seeded random pool slot
+        d["kp"], d["vp"], d["table"] = workloads.page_caches(d["k"], d["v"], page_size, seed=100 + r, spare_pages=64)
+        del d["k"], d["v"]
+    torch.cuda.empty_cache()
+
+    def step_paged(i):
+        s = sets[i % 4] if i >= 0 else sets[0]
+        fa.sdpa_decode_paged(s["q"], s["kp"], s["vp"], s["table"], s["kv_len"], scale=w.scale, out=o, lse=lse,
+                             workspace=ws)
+
+    paged = line("paged_" + w.name, time_steps(step_paged, K, W), 2,
+                 {"page_size": page_size, "pages": "seeded random placement in a pool with 64 spare pages"})
+    return contiguous, paged
 
 
 def bench_e2e_prefill(w, K, dev):
@@ -422,14 +441,21 @@ def profile_run(args):
         x = workloads.decode_inputs(w, pad_value=0.0)
         q, k, v, kvl = (x[n].to(dev) for n in ("q", "k", "v", "kv_len"))
         ws = torch.empty(fa.sdpa_decode_workspace_size(w.B, w.Hq, w.Sk, w.Dv), dtype=torch.uint8, device=dev)
+        if args.page_size:
+            kp, vp, table = workloads.page_caches(k, v, args.page_size, seed=100, spare_pages=64)
+            del k, v
 
-        def step(_i=0):
-            fa.sdpa_decode(q, k, v, kvl, scale=w.scale, workspace=ws)
+            def step(_i=0):
+                fa.sdpa_decode_paged(q, kp, vp, table, kvl, scale=w.scale, workspace=ws)
+        else:
+            def step(_i=0):
+                fa.sdpa_decode(q, k, v, kvl, scale=w.scale, workspace=ws)
     else:
         _, step = prefill_setup(w, dev)
     ms = time_steps(step, max(args.steps, 1), max(args.warmup, 1))
     status = fa.sdpa_status_string(fa.sdpa_check_device_status())
-    print(json.dumps({"profile": w.name, "B": w.B, "ms_per_step": sum(ms) / len(ms), "device_status": status}))
+    print(json.dumps({"profile": w.name, "B": w.B, "page_size": args.page_size or None, "ms_per_step": sum(ms) / len(ms),
+                      "device_status": status}))
 
 
 def main():
@@ -442,6 +468,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", metavar="WORKLOAD", help="only run WORKLOAD's launches (for ncu captures)")
     ap.add_argument("--batch", type=int, default=0, help="with --profile: override the batch size")
+    ap.add_argument("--page-size", type=int, default=0, help="with --profile on the decode: a paged cache of this page size")
     args = ap.parse_args()
     if args.profile:
         profile_run(args)
@@ -494,8 +521,9 @@ def main():
         for name in ("tiny_prefill_f16_d64", "unaligned_mask_prefill_bf16_d128", "mla_fp8_causal_prefill_d192"):
             others[name] = bench_prefill(workloads.WORKLOADS[name], k2, args.warmup, dev, peaks, flusher)
             torch.cuda.empty_cache()
-        others["splitkv_decode_bf16_d128"] = bench_decode(workloads.WORKLOADS["splitkv_decode_bf16_d128"], k2,
-                                                          args.warmup, dev, peaks)
+        dec, dec_paged = bench_decode(workloads.WORKLOADS["splitkv_decode_bf16_d128"], k2, args.warmup, dev, peaks)
+        others[dec["workload"]] = dec
+        others[dec_paged["workload"]] = dec_paged
         torch.cuda.empty_cache()
 
     cpu = None

@@ -11,6 +11,8 @@ Entry points (same names as the C ABI):
     sdpa_fwd(q, k, v, ...)                     fp16 / bf16 prefill
     sdpa_fwd_fp8(q, k, v, dq, dk, dv, ...)     e4m3 prefill with per-tensor scales
     sdpa_decode(q, k_cache, v_cache, kv_len, ...)   two-phase split-KV decode
+    sdpa_decode_paged(q, k_pool, v_pool, page_table, kv_len, ...)   the same over a paged cache
+    sdpa_decode_noalloc(q, k_cache, v_cache, kv_len, ...)   the same with library-owned scratch
     sdpa_fwd_workspace_size, sdpa_decode_workspace_size, sdpa_check_device_status,
     sdpa_status_string, sdpa_version
 """
@@ -207,6 +209,43 @@ def sdpa_decode(q, k_cache, v_cache, kv_len, *, scale: float | None = None, out=
                              Hkv, max_kv, D, Dv, strides, scale, _ptr(workspace),
                              workspace.numel() * workspace.element_size(), _DT[q.dtype], _stream_ptr(stream))
     _check("sdpa_decode", rc)
+    return out, lse
+
+
+def sdpa_decode_paged(q, k_pool, v_pool, page_table, kv_len, *, scale: float | None = None, out=None, lse=None,
+                      return_lse: bool = True, workspace=None, stream=None):
+    """Decode over a paged cache: q [B,Hq,D], pools [n_pages,page_size,Hkv,D|Dv], page_table int32
+    [B, max_pages] (device; logical page -> physical page), kv_len int32 [B] (device)."""
+    if q.dim() != 3 or k_pool.dim() != 4 or v_pool.dim() != 4 or page_table.dim() != 2:
+        raise ValueError("q must be [B, Hq, D], pools [n_pages, page_size, Hkv, D], page_table [B, max_pages]")
+    B, Hq, D = q.shape
+    n_pages, page_size, Hkv, _ = k_pool.shape
+    Dv = v_pool.shape[-1]
+    max_pages = page_table.shape[1]
+    for t, name in ((kv_len, "kv_len"), (page_table, "page_table")):
+        if t.dtype != torch.int32 or not t.is_cuda:
+            raise ValueError(f"{name} must be an int32 CUDA tensor")
+    if page_table.stride(1) != 1:
+        raise ValueError("page_table rows must be contiguous")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty((B, Hq, Dv), dtype=q.dtype, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(sdpa_decode_workspace_size(B, Hq, max_pages * page_size, Dv), dtype=torch.uint8,
+                                device=q.device)
+    strides = _i64([*q.stride()[:2], *k_pool.stride()[:3], *v_pool.stride()[:3], *out.stride()[:2],
+                    page_table.stride(0)])
+    lib = _load()
+    fn = lib.sdpa_decode_paged
+    p, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    fn.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, i, i, i, p, f, p, ctypes.c_size_t, i, p]
+    fn.restype = i
+    rc = fn(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(kv_len), _ptr(out), _ptr(lse), B, Hq, Hkv,
+            page_size, max_pages, n_pages, D, Dv, strides, scale, _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _DT[q.dtype], _stream_ptr(stream))
+    _check("sdpa_decode_paged", rc)
     return out, lse
 
 

@@ -311,6 +311,76 @@ int sdpa_decode(const void* q, const void* k_cache, const void* v_cache, const i
   return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 
+int sdpa_decode_paged(const void* q, const void* k_pool, const void* v_pool, const int32_t* page_table,
+                      const int32_t* kv_len, void* o, float* lse, int B, int Hq, int Hkv, int page_size, int max_pages,
+                      int n_pages, int D, int Dv, const int64_t* strides, float scale, void* workspace,
+                      size_t workspace_bytes, sdpa_dtype dtype, void* stream) {
+  if (!q || !k_pool || !v_pool || !page_table || !kv_len || !o) return SDPA_ERR_INVALID;
+  if (B < 1 || Hq < 1 || Hkv < 1 || page_size < 1 || max_pages < 1 || n_pages < 1 || D < 1 || Dv < 1)
+    return SDPA_ERR_INVALID;
+  if (Hq % Hkv != 0) return SDPA_ERR_INVALID;
+  if (!(std::isfinite(scale) && scale > 0.f)) return SDPA_ERR_INVALID;
+  if (page_size & (page_size - 1)) return SDPA_ERR_INVALID;  // a power of two
+  if (dtype != SDPA_F16 && dtype != SDPA_BF16) return SDPA_ERR_UNSUPPORTED;
+  if (D != 128 || Dv != kDecodeDv) return SDPA_ERR_UNSUPPORTED;
+  if (page_size < 16) return SDPA_ERR_UNSUPPORTED;
+  const int group = Hq / Hkv;
+  if (group > 8) return SDPA_ERR_UNSUPPORTED;
+  if (B > 65535 || Hkv > 65535) return SDPA_ERR_UNSUPPORTED;
+  const long long max_kv_ll = (long long)max_pages * page_size;
+  if (max_kv_ll > (1ll << 30)) return SDPA_ERR_UNSUPPORTED;
+  const int max_kv = (int)max_kv_ll;
+  int64_t st[SDPA_DECODE_PAGED_NSTRIDES];
+  if (strides) {
+    std::memcpy(st, strides, sizeof(st));
+  } else {
+    const int64_t cs[SDPA_DECODE_PAGED_NSTRIDES] = {(int64_t)Hq * D, D, (int64_t)page_size * Hkv * D, (int64_t)Hkv * D, D,
+                                                    (int64_t)page_size * Hkv * Dv, (int64_t)Hkv * Dv, Dv,
+                                                    (int64_t)Hq * Dv, Dv, max_pages};
+    std::memcpy(st, cs, sizeof(st));
+  }
+  for (int i = 0; i < SDPA_DECODE_NSTRIDES; ++i)
+    if (!stride_ok(st[i], 8)) return SDPA_ERR_UNSUPPORTED;
+  if (st[10] < max_pages) return SDPA_ERR_INVALID;  // page-table rows hold max_pages entries
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(o)) return SDPA_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(kv_len) & 3u) || (reinterpret_cast<uintptr_t>(page_table) & 3u))
+    return SDPA_ERR_INVALID;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SDPA_ERR_INVALID;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < sdpa_decode_workspace_size(B, Hq, max_kv, Dv))
+    return SDPA_ERR_INVALID;
+
+  // the pools as [n_pages, page_size, Hkv, .] tensors: a box is min(64, page_size) rows of one page
+  const CUtensorMapDataType dt = dtype == SDPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const int box_rows = page_size < 64 ? page_size : 64;
+  alignas(64) CUtensorMap tk, tv;
+  if (!encode_bshd(&tk, k_pool, dt, 2, n_pages, page_size, Hkv, D, st[2], st[3], st[4], 64, box_rows,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_bshd(&tv, v_pool, dt, 2, n_pages, page_size, Hkv, Dv, st[5], st[6], st[7], 64, box_rows,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+    return SDPA_ERR_CUDA;
+  uint32_t* status = nullptr;
+  if (status_ptr(&status) != cudaSuccess) return SDPA_ERR_CUDA;
+
+  DecodeParams p{};
+  p.q = q, p.k = k_pool, p.v = v_pool, p.kv_len = kv_len, p.o = o, p.lse = lse;
+  p.ws = static_cast<float*>(workspace);
+  p.status = status;
+  p.q_b = st[0], p.q_h = st[1], p.k_b = st[2], p.k_s = st[3], p.k_h = st[4];
+  p.v_b = st[5], p.v_s = st[6], p.v_h = st[7], p.o_b = st[8], p.o_h = st[9];
+  p.B = B, p.Hq = Hq, p.Hkv = Hkv, p.max_kv = max_kv, p.group = group;
+  p.n_splits_max = (max_kv + kDecodeSplit - 1) / kDecodeSplit;
+  p.scale2 = (float)((double)scale * 1.4426950408889634);
+  p.page_table = page_table;
+  p.pt_b = st[10];
+  p.page_size = page_size;
+  p.log2_page = __builtin_ctz((unsigned)page_size);
+  p.max_pages = max_pages;
+  p.n_pages = n_pages;
+  const cudaError_t e =
+      launch_decode(dtype == SDPA_BF16 ? kBF16 : kF16, p, tk, tv, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
 int sdpa_check_device_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SDPA_ERR_CUDA;
   uint32_t word = 0;

@@ -109,7 +109,7 @@ __device__ __forceinline__ uint32_t swz(int row, int unit) {
 
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
 
-template <int ELEM>
+template <int ELEM, bool PAGED>
 __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                    const __grid_constant__ CUtensorMap tm_v,
                                                                    const DecodeParams p) {
@@ -142,25 +142,55 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const __grid_
   const int G = p.group;
 
   if (warp == kDecodeWarps) {
-    // ---------------------------------------------------------- producer
+    // ---------------------------------------------------------- producer (one warp)
+    // A chunk is 4 boxes (the two 64-column halves of K and of V) for contiguous caches and pages
+    // of at least 64 rows: lane 0 issues them.  Pages of fewer rows need 4 x 64 / page_size boxes
+    // per chunk, one page each: lane 0 posts the byte count and the boxes are issued by separate
+    // lanes, so that their page-table reads and issues overlap.
+    const int rows = PAGED ? min(kDecChunk, p.page_size) : kDecChunk;  // rows per box
+    const int nsub = kDecChunk / rows;                                 // boxes per operand half
     if (lane == 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      int c = 0;
-      for (; c < nchunks; ++c) {
-        const int s = c % kDecStages, r = c / kDecStages;
-        if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, abort_flag, p.status)) break;
-        uint8_t* st = smem + s * kDecStageBytes;
-        const int row = start + c * kDecChunk;  // rows past max_kv read as zeros
-        mbar_arrive_expect_tx(&full[s], kDecStageBytes);
-        tma_load_4d(st, &tm_k, &full[s], 0, kvh, row, b);
-        tma_load_4d(st + kDecBox, &tm_k, &full[s], 64, kvh, row, b);
-        tma_load_4d(st + 2 * kDecBox, &tm_v, &full[s], 0, kvh, row, b);
-        tma_load_4d(st + 3 * kDecBox, &tm_v, &full[s], 64, kvh, row, b);
-      }
-      if (c < nchunks)  // aborted: let the copies in flight land
-        for (int j = max(0, c - kDecStages); j < c; ++j) mbar_drain(&full[j % kDecStages], (j / kDecStages) & 1);
     }
+    int c = 0;
+    for (; c < nchunks; ++c) {
+      const int s = c % kDecStages, r = c / kDecStages;
+      uint8_t* st = smem + s * kDecStageBytes;
+      const int row = start + c * kDecChunk;  // rows past max_kv read as zeros
+      if (nsub == 1) {
+        if (lane == 0) {
+          if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, abort_flag, p.status)) break;
+          mbar_arrive_expect_tx(&full[s], kDecStageBytes);
+          int c3 = b, c2 = row;
+          if constexpr (PAGED) {
+            const int lp = row >> p.log2_page;
+            // logical pages past the table read a page index outside the pool: zero rows, masked
+            c3 = lp < p.max_pages ? __ldg(p.page_table + b * p.pt_b + lp) : p.n_pages;
+            c2 = row & (p.page_size - 1);
+          }
+          tma_load_4d(st, &tm_k, &full[s], 0, kvh, c2, c3);
+          tma_load_4d(st + kDecBox, &tm_k, &full[s], 64, kvh, c2, c3);
+          tma_load_4d(st + 2 * kDecBox, &tm_v, &full[s], 0, kvh, c2, c3);
+          tma_load_4d(st + 3 * kDecBox, &tm_v, &full[s], 64, kvh, c2, c3);
+        }
+      } else {
+        if (r > 0 && !mbar_wait_warp(&empty[s], (r - 1) & 1, abort_flag, p.status)) break;
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], kDecStageBytes);
+        __syncwarp();
+        if (lane < 4 * nsub) {
+          const int part = lane & 3, sub = lane >> 2;  // part: K cols 0-63, K 64-127, V 0-63, V 64-127
+          const int key = row + sub * rows;
+          const int lp = key >> p.log2_page;
+          const int phys = lp < p.max_pages ? __ldg(p.page_table + b * p.pt_b + lp) : p.n_pages;
+          // page_size is a power of two >= 16, so every box starts 2 KB-aligned in the stage
+          tma_load_4d(st + part * kDecBox + sub * rows * 128, part < 2 ? &tm_k : &tm_v, &full[s], (part & 1) * 64,
+                      kvh, 0, phys);
+        }
+      }
+    }
+    if (c < nchunks && lane == 0)  // aborted: let the copies in flight land
+      for (int j = max(0, c - kDecStages); j < c; ++j) mbar_drain(&full[j % kDecStages], (j / kDecStages) & 1);
   } else {
     // ---------------------------------------------------------- consumers
     const int g = lane >> 2, t = lane & 3;
@@ -375,6 +405,16 @@ __global__ void __launch_bounds__(128) mask_convert_kernel(const MaskConvertPara
   }
 }
 
+template <int ELEM, bool PAGED>
+cudaError_t launch_split(dim3 grid, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
+                         cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<ELEM, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kDecSmem);
+  if (e != cudaSuccess) return e;
+  decode_split_kernel<ELEM, PAGED><<<grid, kDecThreads, kDecSmem, st>>>(tk, tv, p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_decode(int elem, const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -382,16 +422,14 @@ cudaError_t launch_decode(int elem, const DecodeParams& p, const CUtensorMap& tk
   const dim3 g1(p.n_splits_max, p.Hkv, p.B), g2(p.Hq, p.B);
   cudaError_t e;
   if (elem == kBF16) {
-    if ((e = cudaFuncSetAttribute(decode_split_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  kDecSmem)) != cudaSuccess)
-      return e;
-    decode_split_kernel<kBF16><<<g1, kDecThreads, kDecSmem, st>>>(tk, tv, p);
+    if (p.page_table) e = launch_split<kBF16, true>(g1, tk, tv, p, st);
+    else e = launch_split<kBF16, false>(g1, tk, tv, p, st);
+    if (e != cudaSuccess) return e;
     decode_combine_kernel<kBF16><<<g2, kDecodeDv, 0, st>>>(p);
   } else {
-    if ((e = cudaFuncSetAttribute(decode_split_kernel<kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  kDecSmem)) != cudaSuccess)
-      return e;
-    decode_split_kernel<kF16><<<g1, kDecThreads, kDecSmem, st>>>(tk, tv, p);
+    if (p.page_table) e = launch_split<kF16, true>(g1, tk, tv, p, st);
+    else e = launch_split<kF16, false>(g1, tk, tv, p, st);
+    if (e != cudaSuccess) return e;
     decode_combine_kernel<kF16><<<g2, kDecodeDv, 0, st>>>(p);
   }
   return cudaGetLastError();

@@ -91,6 +91,12 @@ struct DecodeParams {
   int64_t q_b, q_h, k_b, k_s, k_h, v_b, v_s, v_h, o_b, o_h;
   int B, Hq, Hkv, max_kv, group, n_splits_max;
   float scale2;            // scale * log2(e)
+  // paged caches (page_table != null): key row t of sequence b is row t % page_size of physical
+  // page page_table[b * pt_b + t / page_size]; k/v then point at pools [n_pages, page_size, Hkv, .]
+  // and k_b/k_s (v_b/v_s) are the page and row strides
+  const int32_t* page_table;
+  int64_t pt_b;
+  int page_size, log2_page, max_pages, n_pages;
 };
 
 constexpr int kDecodeSplit = 1024;      // keys per phase-1 CTA

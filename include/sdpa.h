@@ -55,6 +55,8 @@ typedef enum { SDPA_F16 = 0, SDPA_BF16 = 1, SDPA_E4M3 = 2 } sdpa_dtype;
 #define SDPA_FWD_NSTRIDES 12
 /* Number of int64 entries in the decode stride array. */
 #define SDPA_DECODE_NSTRIDES 10
+/* Number of int64 entries in the paged-decode stride array. */
+#define SDPA_DECODE_PAGED_NSTRIDES 11
 
 /*
  * sdpa_fwd_workspace_size -- bytes of device scratch sdpa_fwd / sdpa_fwd_fp8 use, for the
@@ -151,6 +153,32 @@ size_t sdpa_decode_workspace_size(int B, int Hq, int max_kv, int Dv);
 int sdpa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_len, void* o, float* lse,
                 int B, int Hq, int Hkv, int max_kv, int D, int Dv, const int64_t* strides, float scale,
                 void* workspace, size_t workspace_bytes, sdpa_dtype dtype, void* stream);
+
+/*
+ * sdpa_decode_paged -- sdpa_decode over a paged K/V cache: key row t of sequence b is row
+ * t % page_size of physical page page_table[b][t / page_size] of a shared page pool.  The pages
+ * leave the layout of a cache to a page table (page "Xe SDPA Forward Mainloop", section
+ * "Arguments / params": an optional page table, page size and pages per sequence are runtime
+ * arguments of the mainloop); the arithmetic is sdpa_decode's, chunk for chunk, so a paged cache
+ * holding the same rows as a contiguous one gives the same result.
+ *
+ *   k_pool, v_pool [n_pages, page_size, Hkv, D | Dv]  dtype, device
+ *   page_table [B, max_pages] int32, DEVICE pointer: physical page of each logical page.  Entries
+ *           for pages at or past ceil(kv_len[b] / page_size) are never used for a visible key; any
+ *           value there (or outside [0, n_pages)) is harmless: such rows read as zeros or are masked.
+ *   kv_len  [B] int32, device; clamped into [0, max_pages * page_size].
+ *   page_size: a power of two >= 16.
+ *   strides: NULL for the layouts above, else 11 element strides
+ *            {q_b, q_h,  k_page, k_row, k_h,  v_page, v_row, v_h,  o_b, o_h,  page_table row}
+ *   workspace: at least sdpa_decode_workspace_size(B, Hq, max_pages * page_size, Dv) bytes.
+ *   Other arguments, limits and results as in sdpa_decode; a page-table row stride below
+ *   max_pages or a page_size that is not a power of two is SDPA_ERR_INVALID, a page_size below
+ *   16 SDPA_ERR_UNSUPPORTED.
+ */
+int sdpa_decode_paged(const void* q, const void* k_pool, const void* v_pool, const int32_t* page_table,
+                      const int32_t* kv_len, void* o, float* lse, int B, int Hq, int Hkv, int page_size, int max_pages,
+                      int n_pages, int D, int Dv, const int64_t* strides, float scale, void* workspace,
+                      size_t workspace_bytes, sdpa_dtype dtype, void* stream);
 
 /*
  * sdpa_decode_noalloc -- sdpa_decode for callers that cannot allocate device memory: code

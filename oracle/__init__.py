@@ -132,3 +132,33 @@ def sdpa_decode(q, k_cache, v_cache, kv_len, *, scale: float, batches=None, nthr
             raise ValueError("oracle_sdpa_decode: invalid arguments")
         o[n], lse[n] = ob[0], lb[0]
     return o, lse
+
+
+def gather_pages(pool, page_table, kv_len):
+    """Contiguous caches [B, max_pages * page_size, Hkv, .] from a paged pool: logical page i of
+    sequence b is pool[page_table[b, i]].  Only pages holding rows below kv_len[b] are taken (the
+    rest of each row stays zero), so table entries past a sequence's pages are never read.
+
+    The reading of a paged cache (page "Xe SDPA Forward Mainloop", section "Arguments / params":
+    a page table, a page size and pages per sequence): key row t of sequence b is row
+    t % page_size of page page_table[b, t / page_size].  The gather is a plain index copy."""
+    pool = torch.as_tensor(pool)
+    table = torch.as_tensor(page_table).cpu().long()
+    kvl = [int(x) for x in (kv_len.tolist() if hasattr(kv_len, "tolist") else kv_len)]
+    n_pages, page_size = pool.shape[0], pool.shape[1]
+    B, max_pages = table.shape
+    out = torch.zeros((B, max_pages * page_size, *pool.shape[2:]), dtype=pool.dtype)
+    for b in range(B):
+        used = (min(kvl[b], max_pages * page_size) + page_size - 1) // page_size
+        for i in range(used):
+            out[b, i * page_size:(i + 1) * page_size] = pool[int(table[b, i])]
+    return out
+
+
+def sdpa_decode_paged(q, k_pool, v_pool, page_table, kv_len, *, scale: float, batches=None,
+                      nthreads: int | None = None):
+    """Decode oracle over a paged cache: the pages are gathered into contiguous caches and the
+    contiguous decode oracle runs on them."""
+    k = gather_pages(k_pool, page_table, kv_len)
+    v = gather_pages(v_pool, page_table, kv_len)
+    return sdpa_decode(q, k, v, kv_len, scale=scale, batches=batches, nthreads=nthreads)

@@ -80,3 +80,76 @@ def test_decode_rejects_bad_workspace():
     with pytest.raises(fa.SdpaError) as e:
         fa.sdpa_decode(x["q"].to(DEV), x["k"].to(DEV), x["v"].to(DEV), x["kv_len"].to(DEV), workspace=ws)
     assert e.value.status == fa.SDPA_ERR_INVALID
+
+
+def _paged(x, page_size, spare=5, garbage=True, seed=11):
+    kp, vp, table = workloads.page_caches(x["k"], x["v"], page_size, seed=seed, spare_pages=spare)
+    if garbage:
+        # entries past each sequence's pages are never used for a visible key: make them wild
+        for b, L in enumerate(x["kv_len"].tolist()):
+            used = (int(L) + page_size - 1) // page_size
+            table[b, used:] = torch.tensor([-7, 1 << 30, kp.shape[0], 3], dtype=torch.int32).repeat(64)[: table.shape[1] - used]
+    return kp, vp, table
+
+
+@pytest.mark.parametrize("page_size", [16, 32, 64, 128, 256])
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (8, 1)])
+def test_paged_decode_matches_oracle(page_size, Hq, Hkv):
+    lens = [0, 1, 15, 16, 63, 64, 65, 1023, 1024, 1025, 3000]
+    w = W.with_shape(B=len(lens), Hq=Hq, Hkv=Hkv, Sk=4096)
+    x = workloads.decode_inputs(w, kv_len=lens)
+    kp, vp, table = _paged(x, page_size)
+    o, lse = fa.sdpa_decode_paged(x["q"].to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV), x["kv_len"].to(DEV),
+                                  scale=w.scale)
+    torch.cuda.synchronize()
+    assert fa.sdpa_check_device_status() == fa.SDPA_OK
+    ref_o, ref_lse = oracle.sdpa_decode_paged(x["q"], kp, vp, table, x["kv_len"], scale=w.scale)
+    assert_close(o.float().cpu().numpy(), ref_o, TOL_16BIT)
+    assert_lse_close(lse.cpu().numpy(), ref_lse, TOL_LSE_BF16)
+    assert torch.all(o[0] == 0) and torch.all(torch.isneginf(lse[0]))
+
+
+@pytest.mark.parametrize("page_size", [16, 64, 512])
+def test_paged_decode_equals_contiguous_decode(page_size):
+    # paging changes only where the rows come from: chunk for chunk the same arithmetic
+    w = W.with_shape(B=6, Sk=8192)
+    x = workloads.decode_inputs(w, kv_len=[8192, 5000, 1, 4097, 1024, 777], pad_value=0.0)
+    kp, vp, table = _paged(x, page_size, garbage=False)
+    o_c, lse_c = _run(x, w.scale)
+    o_p, lse_p = fa.sdpa_decode_paged(x["q"].to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV), x["kv_len"].to(DEV),
+                                      scale=w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o_p, o_c) and torch.equal(lse_p, lse_c)
+
+
+def test_paged_decode_workload_sampled_sequences():
+    # the decode workload's caches in 64-row pages scattered over the pool
+    x = workloads.decode_inputs(W, pad_value=float("nan"))
+    dev_k, dev_v = x["k"].to(DEV), x["v"].to(DEV)
+    kp, vp, table = workloads.page_caches(dev_k, dev_v, 64, seed=3, spare_pages=17)
+    del dev_k, dev_v
+    o, lse = fa.sdpa_decode_paged(x["q"].to(DEV), kp, vp, table, x["kv_len"].to(DEV), scale=W.scale)
+    torch.cuda.synchronize()
+    assert fa.sdpa_check_device_status() == fa.SDPA_OK
+    kv = x["kv_len"].numpy()
+    pick = sorted({int(np.argmin(kv)), int(np.argmax(kv)), 0, 33, W.B - 1})
+    ref_o, ref_lse = oracle.sdpa_decode(x["q"], x["k"], x["v"], x["kv_len"], scale=W.scale, batches=pick)
+    assert_close(o[pick].float().cpu().numpy(), ref_o, TOL_16BIT)
+    assert_lse_close(lse[pick].cpu().numpy(), ref_lse)
+    assert torch.isfinite(o).all()
+
+
+def test_paged_decode_rejects_bad_arguments():
+    w = W.with_shape(B=2, Sk=256)
+    x = workloads.decode_inputs(w, kv_len=[10, 20], pad_value=0.0)
+    kp, vp, table = _paged(x, 16, garbage=False)
+    args = dict(q=x["q"].to(DEV), k_pool=kp.to(DEV), v_pool=vp.to(DEV), page_table=table.to(DEV),
+                kv_len=x["kv_len"].to(DEV))
+    with pytest.raises(fa.SdpaError):   # page_size 8: below the 16-row minimum
+        kp8, vp8, t8 = _paged(x, 8, garbage=False)
+        fa.sdpa_decode_paged(args["q"], kp8.to(DEV), vp8.to(DEV), t8.to(DEV), args["kv_len"], scale=w.scale)
+    with pytest.raises(fa.SdpaError):   # page_size 48: not a power of two
+        k48 = torch.zeros((12, 48, w.Hkv, 128), dtype=x["k"].dtype, device=DEV)
+        fa.sdpa_decode_paged(args["q"], k48, k48, table[:, :6].contiguous().to(DEV), args["kv_len"], scale=w.scale)
+    torch.cuda.synchronize()
+    assert fa.sdpa_check_device_status() == fa.SDPA_OK

@@ -249,6 +249,31 @@ def test_decode_matches_torch_per_sequence():
     assert np.array_equal(o2[0], o[2]) and np.array_equal(o2[1], o[0])
 
 
+@pytest.mark.parametrize("page_size", [16, 64])
+def test_paged_decode_equals_contiguous_for_any_page_placement(page_size):
+    # the paged oracle gathers pages through the table; any physical placement of the same rows,
+    # garbage in spare pages and in table entries past a sequence's pages must not change the result
+    w = workloads.WORKLOADS["splitkv_decode_bf16_d128"].with_shape(B=3, Hq=4, Hkv=2, Sk=256)
+    x = workloads.decode_inputs(w, kv_len=[1, 100, 256], pad_value=float("nan"))
+    kp, vp, table = workloads.page_caches(x["k"], x["v"], page_size, seed=5, spare_pages=7)
+    used = [(int(L) + page_size - 1) // page_size for L in x["kv_len"]]
+    for b, u in enumerate(used):
+        table[b, u:] = -123456  # never read: past the sequence's pages
+    ref_o, ref_lse = oracle.sdpa_decode(x["q"], x["k"], x["v"], x["kv_len"], scale=w.scale)
+    o, lse = oracle.sdpa_decode_paged(x["q"], kp, vp, table, x["kv_len"], scale=w.scale)
+    assert np.array_equal(o, ref_o) and np.array_equal(lse, ref_lse)
+    # attention does not depend on key order, so swapping two fully used pages must not change a
+    # row, while pointing a used entry at another sequence's page must
+    t2 = table.clone()
+    t2[2, 0], t2[2, 1] = table[2, 1], table[2, 0]
+    o2, _ = oracle.sdpa_decode_paged(x["q"], kp, vp, t2, x["kv_len"], scale=w.scale)
+    assert np.allclose(o2[2], ref_o[2], rtol=0, atol=1e-12)
+    t3 = table.clone()
+    t3[2, 0] = table[1, 0]
+    o3, _ = oracle.sdpa_decode_paged(x["q"], kp, vp, t3, x["kv_len"], scale=w.scale)
+    assert not np.allclose(o3[2], ref_o[2])
+
+
 def test_e4m3_inputs_are_codes_times_scale():
     # the oracle reads e4m3 codes through torch's float8 cast, times the per-tensor scale
     x = torch.tensor([0.0, 1.0, -2.5, 448.0, 0.001953125, -0.875], dtype=torch.float32)

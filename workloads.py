@@ -161,6 +161,29 @@ def decode_inputs(w: Workload, rotation: int = 0, pad_value: float = float("nan"
     return {"q": q, "k": k, "v": v, "kv_len": kv_len}
 
 
+def page_caches(k, v, page_size: int, seed: int, spare_pages: int = 0):
+    """Scatter contiguous caches [B, max_kv, Hkv, .] into page pools [n_pages, page_size, Hkv, .].
+
+    Logical page i of sequence b goes to physical page perm[b * max_pages + i] of a seeded random
+    permutation over n_pages = B * max_pages + spare_pages; spare pages hold NaN.  The table is
+    int32 [B, max_pages].  Works on any device (torch indexing only); max_kv must be a multiple of
+    page_size."""
+    B, max_kv = k.shape[0], k.shape[1]
+    assert max_kv % page_size == 0
+    max_pages = max_kv // page_size
+    n_pages = B * max_pages + spare_pages
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    perm = torch.randperm(n_pages, generator=g)[: B * max_pages].to(k.device)
+    pools = []
+    for c in (k, v):
+        pool = torch.full((n_pages, page_size, *c.shape[2:]), float("nan"), dtype=c.dtype, device=c.device)
+        pool[perm] = c.reshape(B * max_pages, page_size, *c.shape[2:])
+        pools.append(pool)
+    table = perm.view(B, max_pages).to(torch.int32)
+    return pools[0], pools[1], table
+
+
 def custom_prefill(B, Hq, Hkv, Sq, Sk, D, Dv, dtype="bf16", dist="normal", seed=0, mask=False,
                    masked_frac=0.1, full_row_frac=0.05):
     """Small prefill cases for tests: same recipe, explicit seed."""
