@@ -58,6 +58,10 @@ def prefill_flops(w) -> float:
     return 2.0 * (w.D + w.Dv) * w.B * w.Hq * visible_pairs(w.Sq, w.Sk, w.causal)
 
 
+def varlen_flops(w, lengths) -> float:
+    return sum(2.0 * (w.D + w.Dv) * w.Hq * visible_pairs(L, L, w.causal) for L in lengths)
+
+
 def decode_bytes(w, kv_len) -> float:
     esz = 2
     kv = float(np.sum(np.asarray(kv_len, dtype=np.int64))) * w.Hkv * (w.D + w.Dv) * esz
@@ -230,6 +234,37 @@ def bench_prefill(w, K, W, dev, peaks, flusher):
         r["roofline"] = {"bound": "tensor", "achieved": tflops, "peak": bf16, "unit": "TFLOP/s", "frac": tflops / bf16,
                          "peak_note": "bf16 burst, of " + peaks["source"], "traffic": recorded_traffic(w.name)}
     return r
+
+
+def varlen_setup(w, dev, rotation=0):
+    import flash_attention_forward_gb300 as fa
+
+    x = workloads.varlen_inputs(w, rotation)
+    q, k, v, cu_q, cu_k = (x[n].to(dev) for n in ("q", "k", "v", "cu_q", "cu_k"))
+    total_q = q.shape[0]
+    o = torch.empty((total_q, w.Hq, w.Dv), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.Hq, total_q), dtype=torch.float32, device=dev)
+    ws = torch.empty(fa.sdpa_fwd_varlen_workspace_size(w.B), dtype=torch.uint8, device=dev)
+    max_q = max(x["lengths"])
+
+    def step(_i=0):
+        fa.sdpa_fwd_varlen(q, k, v, cu_q, cu_k, max_q, scale=w.scale, causal=w.causal, out=o, lse=lse, workspace=ws)
+
+    return x, step
+
+
+def bench_varlen(w, K, W, dev, peaks, flusher):
+    """Packed sequences of the drawn lengths: one tile-prefix scan and one prefill per step."""
+    x, step = varlen_setup(w, dev)
+    ms = time_steps(step, K, W, flusher)
+    flops = varlen_flops(w, x["lengths"])
+    avg = sum(ms) / len(ms)
+    tflops = flops / (avg * 1e-3) / 1e12
+    bf16 = peaks["bf16_tflops"]
+    return {"workload": w.name, "value": tflops, "unit": "TFLOP/s", "ms_per_step": avg, "flops_per_step": flops,
+            "launches_per_step": 2, "sequences": w.B, "total_tokens": int(sum(x["lengths"])),
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": bf16, "unit": "TFLOP/s", "frac": tflops / bf16,
+                         "peak_note": "bf16 burst, of " + peaks["source"], "traffic": recorded_traffic(w.name)}}
 
 
 def bench_decode(w, K, W, dev, peaks, page_size: int = 64):
@@ -450,6 +485,8 @@ def profile_run(args):
         else:
             def step(_i=0):
                 fa.sdpa_decode(q, k, v, kvl, scale=w.scale, workspace=ws)
+    elif w.kind == "varlen":
+        _, step = varlen_setup(w, dev)
     else:
         _, step = prefill_setup(w, dev)
     ms = time_steps(step, max(args.steps, 1), max(args.warmup, 1))
@@ -521,6 +558,9 @@ def main():
         for name in ("tiny_prefill_f16_d64", "unaligned_mask_prefill_bf16_d128", "mla_fp8_causal_prefill_d192"):
             others[name] = bench_prefill(workloads.WORKLOADS[name], k2, args.warmup, dev, peaks, flusher)
             torch.cuda.empty_cache()
+        vw = workloads.WORKLOADS["varlen_causal_prefill_bf16_d128"]
+        others[vw.name] = bench_varlen(vw, k2, args.warmup, dev, peaks, flusher)
+        torch.cuda.empty_cache()
         dec, dec_paged = bench_decode(workloads.WORKLOADS["splitkv_decode_bf16_d128"], k2, args.warmup, dev, peaks)
         others[dec["workload"]] = dec
         others[dec_paged["workload"]] = dec_paged

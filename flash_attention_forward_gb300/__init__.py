@@ -10,10 +10,13 @@ computation runs in the library's kernels; there is no fallback.
 Entry points (same names as the C ABI):
     sdpa_fwd(q, k, v, ...)                     fp16 / bf16 prefill
     sdpa_fwd_fp8(q, k, v, dq, dk, dv, ...)     e4m3 prefill with per-tensor scales
+    sdpa_fwd_varlen(q, k, v, cu_q, cu_k, max_seqlen_q, ...)   prefill of packed sequences
+    sdpa_fwd_varlen_fp8(q, k, v, cu_q, cu_k, max_seqlen_q, dq, dk, dv, ...)   the same in e4m3
     sdpa_decode(q, k_cache, v_cache, kv_len, ...)   two-phase split-KV decode
     sdpa_decode_paged(q, k_pool, v_pool, page_table, kv_len, ...)   the same over a paged cache
     sdpa_decode_noalloc(q, k_cache, v_cache, kv_len, ...)   the same with library-owned scratch
-    sdpa_fwd_workspace_size, sdpa_decode_workspace_size, sdpa_check_device_status,
+    sdpa_fwd_workspace_size, sdpa_fwd_varlen_workspace_size, sdpa_decode_workspace_size,
+    sdpa_check_device_status,
     sdpa_status_string, sdpa_version
 """
 from __future__ import annotations
@@ -60,6 +63,13 @@ def _load():
         lib.sdpa_fwd.restype = i
         lib.sdpa_fwd_fp8.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, p, f, i, p, p, p, sz, f, f, f, i, p]
         lib.sdpa_fwd_fp8.restype = i
+        lib.sdpa_fwd_varlen_workspace_size.argtypes = [i]
+        lib.sdpa_fwd_varlen_workspace_size.restype = sz
+        lib.sdpa_fwd_varlen.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, i, i, i, p, f, i, p, sz, i, i, p]
+        lib.sdpa_fwd_varlen.restype = i
+        lib.sdpa_fwd_varlen_fp8.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, i, i, i, p, f, i, p, sz, f, f, f, i,
+                                            p]
+        lib.sdpa_fwd_varlen_fp8.restype = i
         lib.sdpa_decode_workspace_size.argtypes = [i, i, i, i]
         lib.sdpa_decode_workspace_size.restype = sz
         lib.sdpa_decode.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, p, f, p, sz, i, p]
@@ -183,6 +193,75 @@ def sdpa_fwd_fp8(q, k, v, descale_q: float, descale_k: float, descale_v: float, 
                               float(descale_q), float(descale_k), float(descale_v), _DT[out.dtype],
                               _stream_ptr(stream))
     _check("sdpa_fwd_fp8", rc)
+    return out, lse
+
+
+def sdpa_fwd_varlen_workspace_size(B: int) -> int:
+    """Bytes of workspace a packed prefill of B sequences needs (the per-sequence tile prefix)."""
+    return int(_load().sdpa_fwd_varlen_workspace_size(B))
+
+
+def _varlen_args(q, k, v, cu_seqlens_q, cu_seqlens_k, out, lse, workspace, out_dtype, return_lse):
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
+        raise ValueError("q, k, v must be packed [total, H, D]")
+    total_q, Hq, D = q.shape
+    total_k, Hkv, _ = k.shape
+    Dv = v.shape[-1]
+    for t in (q, k, v):
+        if not t.is_cuda or t.stride(-1) != 1:
+            raise ValueError("q, k, v must be CUDA tensors with unit innermost stride")
+    for t, name in ((cu_seqlens_q, "cu_seqlens_q"), (cu_seqlens_k, "cu_seqlens_k")):
+        if t.dtype != torch.int32 or not t.is_cuda or t.dim() != 1 or t.stride(0) != 1:
+            raise ValueError(f"{name} must be a contiguous int32 CUDA vector")
+    B = cu_seqlens_q.numel() - 1
+    if cu_seqlens_k.numel() != B + 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both hold B + 1 offsets")
+    if out is None:
+        out = torch.empty((total_q, Hq, Dv), dtype=out_dtype, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
+    if lse is not None and (tuple(lse.shape) != (Hq, total_q) or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous fp32 [Hq, total_q] tensor")
+    if workspace is None:
+        workspace = torch.empty(max(16, sdpa_fwd_varlen_workspace_size(B)), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    strides = _i64([*q.stride()[:2], *k.stride()[:2], *v.stride()[:2], *out.stride()[:2]])
+    return B, total_q, total_k, Hq, Hkv, D, Dv, out, lse, strides, workspace, ws_bytes
+
+
+def sdpa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, *, scale: float | None = None,
+                    causal: bool = False, out=None, lse=None, return_lse: bool = True, workspace=None, stream=None):
+    """Prefill of B sequences packed back to back: q [total_q,Hq,D], k [total_k,Hkv,D], v [total_k,Hkv,Dv]
+    (fp16/bf16); sequence b owns rows cu_seqlens_q[b]..cu_seqlens_q[b+1]-1 (keys likewise), both
+    int32 [B+1] on the device; max_seqlen_q bounds every query length.  Causal masking is top-left
+    within each sequence.  Returns (o [total_q,Hq,Dv], lse [Hq,total_q] fp32 or None)."""
+    if q.dtype not in (torch.float16, torch.bfloat16):
+        raise ValueError("sdpa_fwd_varlen takes fp16 or bf16 inputs (use sdpa_fwd_varlen_fp8 for e4m3)")
+    scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
+    B, total_q, total_k, Hq, Hkv, D, Dv, out, lse, strides, workspace, ws_bytes = _varlen_args(
+        q, k, v, cu_seqlens_q, cu_seqlens_k, out, lse, workspace, q.dtype, return_lse)
+    rc = _load().sdpa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q),
+                                 _ptr(cu_seqlens_k), B, Hq, Hkv, total_q, total_k, int(max_seqlen_q), D, Dv, strides,
+                                 scale, int(bool(causal)), _ptr(workspace), ws_bytes, _DT[q.dtype], _DT[out.dtype],
+                                 _stream_ptr(stream))
+    _check("sdpa_fwd_varlen", rc)
+    return out, lse
+
+
+def sdpa_fwd_varlen_fp8(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, descale_q: float,
+                        descale_k: float, descale_v: float, *, scale: float | None = None, causal: bool = False,
+                        out=None, lse=None, return_lse: bool = True, workspace=None, stream=None):
+    """sdpa_fwd_varlen with e4m3 codes and per-tensor scales.  Returns (o bf16, lse fp32 or None)."""
+    if q.dtype != torch.float8_e4m3fn:
+        raise ValueError("sdpa_fwd_varlen_fp8 takes float8_e4m3fn inputs")
+    scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
+    B, total_q, total_k, Hq, Hkv, D, Dv, out, lse, strides, workspace, ws_bytes = _varlen_args(
+        q, k, v, cu_seqlens_q, cu_seqlens_k, out, lse, workspace, torch.bfloat16, return_lse)
+    rc = _load().sdpa_fwd_varlen_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q),
+                                     _ptr(cu_seqlens_k), B, Hq, Hkv, total_q, total_k, int(max_seqlen_q), D, Dv,
+                                     strides, scale, int(bool(causal)), _ptr(workspace), ws_bytes, float(descale_q),
+                                     float(descale_k), float(descale_v), _DT[out.dtype], _stream_ptr(stream))
+    _check("sdpa_fwd_varlen_fp8", rc)
     return out, lse
 
 

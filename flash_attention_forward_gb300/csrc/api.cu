@@ -99,10 +99,31 @@ SplitPlan fwd_split_plan(int B, int Hq, int Sq, int Sk, bool causal) {
   return prefill_split_plan(items, sms, (Sk + kBlockK - 1) / kBlockK, causal);
 }
 
+// Packed variable-length sequences: sequence b owns query rows cu_q[b] .. cu_q[b + 1] and key
+// rows cu_k[b] .. cu_k[b + 1] of [total, H, D] tensors.
+struct VarlenArgs {
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int total_q, total_k, max_seqlen_q;
+};
+
+size_t varlen_ws_bytes(int B) { return round16((size_t)(B + 1) * sizeof(int32_t)); }
+
+// Work tiles a varlen launch is sized for: no sequence is longer than max_seqlen_q, and the
+// lengths add up to at most total_q.
+long long varlen_max_tiles(int B, int total_q, int max_seqlen_q) {
+  const long long by_max = (long long)B * ((max_seqlen_q + kCtaRows - 1) / kCtaRows);
+  const long long by_total = ((long long)total_q + (long long)(kCtaRows - 1) * B) / kCtaRows;
+  return by_max < by_total ? by_max : by_total;
+}
+
+// Shared body of the dense and packed entry points (vl != null: B sequences packed as
+// described by *vl; Sq, Sk are then the longest query length and total_k).
 int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,
                int Sk, int D, int Dv, const int64_t* strides, float scale, int causal, const void* mask,
                const int64_t* mask_strides, void* workspace, size_t workspace_bytes, int elem, float descale_q,
-               float descale_k, float descale_v, sdpa_dtype out_dtype, void* stream) {
+               float descale_k, float descale_v, sdpa_dtype out_dtype, void* stream,
+               const VarlenArgs* vl = nullptr) {
   // ---- validation (no CUDA call before this block passes)
   if (!q || !k || !v || !o) return SDPA_ERR_INVALID;
   if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Sk < 1 || D < 1 || Dv < 1) return SDPA_ERR_INVALID;
@@ -121,7 +142,18 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
       return SDPA_ERR_UNSUPPORTED;
   }
   int64_t st[SDPA_FWD_NSTRIDES];
-  if (strides) {
+  if (vl) {
+    // (row, head) strides per tensor; the batch dimension of the tensor maps has extent 1
+    int64_t r[SDPA_FWD_VARLEN_NSTRIDES] = {(int64_t)Hq * D, D, (int64_t)Hkv * D, D,
+                                          (int64_t)Hkv * Dv, Dv, (int64_t)Hq * Dv, Dv};
+    if (strides) std::memcpy(r, strides, sizeof(r));
+    const int64_t rows[4] = {vl->total_q, vl->total_k, vl->total_k, vl->total_q};
+    for (int t = 0; t < 4; ++t) {
+      st[3 * t] = r[2 * t] * rows[t];
+      st[3 * t + 1] = r[2 * t];
+      st[3 * t + 2] = r[2 * t + 1];
+    }
+  } else if (strides) {
     std::memcpy(st, strides, sizeof(st));
   } else {
     const int64_t cs[SDPA_FWD_NSTRIDES] = {(int64_t)Sq * Hq * D,  (int64_t)Hq * D,  D,
@@ -139,8 +171,14 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SDPA_ERR_INVALID;
   const int n_kblocks = (Sk + kBlockK - 1) / kBlockK;
   const int n_cta_tiles = (Sq + kCtaRows - 1) / kCtaRows;
-  const long long n_items = (long long)n_cta_tiles * B * Hq;
+  const long long n_items = vl ? varlen_max_tiles(B, vl->total_q, vl->max_seqlen_q) * Hq
+                               : (long long)n_cta_tiles * B * Hq;
   if (n_items * kMaxSplitParts >= (1ll << 31)) return SDPA_ERR_UNSUPPORTED;
+  if (vl) {
+    if (!vl->cu_q || !vl->cu_k || mask) return SDPA_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(vl->cu_q) | reinterpret_cast<uintptr_t>(vl->cu_k)) & 3u) return SDPA_ERR_INVALID;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < varlen_ws_bytes(B)) return SDPA_ERR_INVALID;
+  }
   int64_t mb = 0, mi = 0;
   if (mask) {
     if (reinterpret_cast<uintptr_t>(mask) & 1u) return SDPA_ERR_INVALID;
@@ -152,7 +190,7 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   // the key-range split of the tail runs only when the caller's workspace also holds its
   // partial results (sdpa_fwd_workspace_size includes them)
   const size_t mask_bytes = mask ? mask_ws_bytes(B, Sq, Sk) : 0;
-  SplitPlan sp = fwd_split_plan(B, Hq, Sq, Sk, causal != 0);
+  SplitPlan sp = vl ? SplitPlan{} : fwd_split_plan(B, Hq, Sq, Sk, causal != 0);
   const size_t split_bytes = prefill_split_bytes(sp, Dv);
   if (split_bytes == 0 || !workspace || !aligned16(workspace) || workspace_bytes < mask_bytes + split_bytes)
     sp = SplitPlan{};
@@ -163,12 +201,13 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const CUtensorMapSwizzle sw_qk = elem == kE4M3 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
   alignas(64) CUtensorMap tq, tk, tv;
-  if (!encode_bshd(&tq, q, dt, esize, B, Sq, Hq, D, st[0], st[1], st[2], 64, kBlockQ, sw_qk)) return SDPA_ERR_CUDA;
-  if (!encode_bshd(&tk, k, dt, esize, B, Sk, Hkv, D, st[3], st[4], st[5], 64, kBlockK, sw_qk)) return SDPA_ERR_CUDA;
+  const int mB = vl ? 1 : B, mSq = vl ? vl->total_q : Sq, mSk = vl ? vl->total_k : Sk;  // tensor-map extents
+  if (!encode_bshd(&tq, q, dt, esize, mB, mSq, Hq, D, st[0], st[1], st[2], 64, kBlockQ, sw_qk)) return SDPA_ERR_CUDA;
+  if (!encode_bshd(&tk, k, dt, esize, mB, mSk, Hkv, D, st[3], st[4], st[5], 64, kBlockK, sw_qk)) return SDPA_ERR_CUDA;
   const bool v_ok = elem == kE4M3
-                        ? encode_bshd(&tv, v, dt, 1, B, Sk, Hkv, Dv, st[6], st[7], st[8], Dv, kBlockK,
+                        ? encode_bshd(&tv, v, dt, 1, mB, mSk, Hkv, Dv, st[6], st[7], st[8], Dv, kBlockK,
                                       CU_TENSOR_MAP_SWIZZLE_NONE)
-                        : encode_bshd(&tv, v, dt, 2, B, Sk, Hkv, Dv, st[6], st[7], st[8], 64, kBlockK,
+                        : encode_bshd(&tv, v, dt, 2, mB, mSk, Hkv, Dv, st[6], st[7], st[8], 64, kBlockK,
                                       CU_TENSOR_MAP_SWIZZLE_128B);
   if (!v_ok) return SDPA_ERR_CUDA;
 
@@ -211,6 +250,16 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
     p.mask = static_cast<const uint16_t*>(mask);
     p.mask_b = mb, p.mask_i = mi;
   }
+  if (vl) {
+    int32_t* prefix = static_cast<int32_t*>(workspace);
+    VarlenPrepParams vp{vl->cu_q, vl->cu_k, B, vl->total_q, vl->total_k, (int)(n_items / Hq), prefix, status};
+    if (launch_varlen_prep(vp, stm) != cudaSuccess) return SDPA_ERR_CUDA;
+    p.varlen = 1;
+    p.total_q = vl->total_q;
+    p.cu_q = vl->cu_q;
+    p.cu_k = vl->cu_k;
+    p.tile_prefix = prefix;
+  }
   bool supported = false;
   cudaError_t e;
   if (elem == kE4M3)
@@ -252,6 +301,42 @@ int sdpa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* ls
                  float descale_k, float descale_v, sdpa_dtype out_dtype, void* stream) {
   return fwd_common(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, Dv, strides, scale, causal, mask, mask_strides,
                     workspace, workspace_bytes, kE4M3, descale_q, descale_k, descale_v, out_dtype, stream);
+}
+
+size_t sdpa_fwd_varlen_workspace_size(int B) { return B < 1 ? 0 : varlen_ws_bytes(B); }
+
+namespace {
+int fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens_q,
+               const int32_t* cu_seqlens_k, int B, int Hq, int Hkv, int total_q, int total_k, int max_seqlen_q,
+               int D, int Dv, const int64_t* strides, float scale, int causal, void* workspace,
+               size_t workspace_bytes, int elem, float descale_q, float descale_k, float descale_v,
+               sdpa_dtype out_dtype, void* stream) {
+  if (B < 1 || total_q < 1 || total_k < 1 || max_seqlen_q < 1 || max_seqlen_q > total_q) return SDPA_ERR_INVALID;
+  const VarlenArgs vl{cu_seqlens_q, cu_seqlens_k, total_q, total_k, max_seqlen_q};
+  return fwd_common(q, k, v, o, lse, B, Hq, Hkv, max_seqlen_q, total_k, D, Dv, strides, scale,
+                    causal, nullptr, nullptr, workspace, workspace_bytes, elem, descale_q, descale_k, descale_v,
+                    out_dtype, stream, &vl);
+}
+}  // namespace
+
+int sdpa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens_q,
+                    const int32_t* cu_seqlens_k, int B, int Hq, int Hkv, int total_q, int total_k, int max_seqlen_q,
+                    int D, int Dv, const int64_t* strides, float scale, int causal, void* workspace,
+                    size_t workspace_bytes, sdpa_dtype in_dtype, sdpa_dtype out_dtype, void* stream) {
+  if (in_dtype != SDPA_F16 && in_dtype != SDPA_BF16) return SDPA_ERR_UNSUPPORTED;
+  return fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv, total_q, total_k, max_seqlen_q, D, Dv,
+                    strides, scale, causal, workspace, workspace_bytes, in_dtype == SDPA_BF16 ? kBF16 : kF16, 1.f,
+                    1.f, 1.f, out_dtype, stream);
+}
+
+int sdpa_fwd_varlen_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
+                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int B, int Hq, int Hkv, int total_q,
+                        int total_k, int max_seqlen_q, int D, int Dv, const int64_t* strides, float scale, int causal,
+                        void* workspace, size_t workspace_bytes, float descale_q, float descale_k, float descale_v,
+                        sdpa_dtype out_dtype, void* stream) {
+  return fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv, total_q, total_k, max_seqlen_q, D, Dv,
+                    strides, scale, causal, workspace, workspace_bytes, kE4M3, descale_q, descale_k, descale_v,
+                    out_dtype, stream);
 }
 
 size_t sdpa_decode_workspace_size(int B, int Hq, int max_kv, int Dv) {
@@ -388,7 +473,8 @@ int sdpa_check_device_status(void* stream) {
   if (word == 0) return SDPA_OK;
   const uint32_t zero = 0;
   if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return SDPA_ERR_CUDA;
-  return (word & kStatusTimeout) ? SDPA_ERR_TIMEOUT : SDPA_ERR_CUDA;
+  if (word & kStatusTimeout) return SDPA_ERR_TIMEOUT;
+  return (word & kStatusBadSeqlens) ? SDPA_ERR_INVALID : SDPA_ERR_CUDA;
 }
 
 const char* sdpa_status_string(int status) {

@@ -405,6 +405,62 @@ __global__ void __launch_bounds__(128) mask_convert_kernel(const MaskConvertPara
   }
 }
 
+// Work-tile prefix of packed variable-length sequences: tile_prefix[b] is the number of work
+// tiles (2 x 128 query rows) of the sequences before b, tile_prefix[B] of all of them.  One CTA
+// scans the B counts 1024 at a time.  Offsets that are not non-decreasing within [0, total], or
+// more tiles than the launch was sized for, raise kStatusBadSeqlens and leave every count zero,
+// so the prefill that follows stores nothing.
+__global__ void __launch_bounds__(1024) varlen_prep_kernel(const VarlenPrepParams p) {
+  __shared__ long long warp_sum[32];  // 64-bit sums: invalid offsets must not overflow them
+  __shared__ long long carry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  int bad = 0;
+  for (int base = 0; base < p.B; base += 1024) {
+    const int b = base + tid;
+    long long v = 0;
+    if (b < p.B) {
+      const int q0 = __ldg(p.cu_q + b), q1 = __ldg(p.cu_q + b + 1);
+      const int k0 = __ldg(p.cu_k + b), k1 = __ldg(p.cu_k + b + 1);
+      if (q1 < q0 || k1 < k0) bad = 1;
+      if (b == 0 && (q0 < 0 || k0 < 0)) bad = 1;
+      if (b == p.B - 1 && (q1 > p.total_q || k1 > p.total_k)) bad = 1;
+      v = (max(0ll, (long long)q1 - q0) + kCtaRows - 1) / kCtaRows;
+    }
+    long long x = v;  // inclusive scan inside the warp
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, x, d);
+      if (lane >= d) x += y;
+    }
+    if (lane == 31) warp_sum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      long long w = warp_sum[lane];
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, w, d);
+        if (lane >= d) w += y;
+      }
+      warp_sum[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    const long long incl = x + (warp > 0 ? warp_sum[warp - 1] : 0ll);
+    if (b < p.B) p.tile_prefix[b] = static_cast<int32_t>(carry + incl - v);
+    __syncthreads();
+    if (tid == 1023) carry += incl;
+    __syncthreads();
+  }
+  const bool fail = __syncthreads_or(bad) || carry > p.max_tiles;
+  if (fail) {
+    for (int b = tid; b <= p.B; b += 1024) p.tile_prefix[b] = 0;
+    if (tid == 0) atomicOr(p.status, kStatusBadSeqlens);
+  } else if (tid == 0) {
+    p.tile_prefix[p.B] = static_cast<int32_t>(carry);
+  }
+}
+
 template <int ELEM, bool PAGED>
 cudaError_t launch_split(dim3 grid, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                          cudaStream_t st) {
@@ -439,6 +495,11 @@ cudaError_t launch_mask_convert(const MaskConvertParams& p, cudaStream_t st) {
   const int64_t warps = (int64_t)p.B * p.Sq * ((p.n_kblocks + kMaskGroup - 1) / kMaskGroup);
   if ((warps + 3) / 4 > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
   mask_convert_kernel<<<(unsigned)((warps + 3) / 4), 128, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_varlen_prep(const VarlenPrepParams& p, cudaStream_t st) {
+  varlen_prep_kernel<<<1, 1024, 0, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -10,7 +10,7 @@
 namespace sdpa {
 
 // Status bits a kernel ORs into the device status word.
-enum : uint32_t { kStatusTimeout = 1u };
+enum : uint32_t { kStatusTimeout = 1u, kStatusBadSeqlens = 2u };
 
 // Prefill tile geometry shared by host and device.
 constexpr int kBlockQ = 128;           // query rows per tile (one TMEM lane each)
@@ -46,6 +46,22 @@ struct PrefillParams {
   int n_units, n_full, split_tail, split_parts;
   float* split_o;          // [split_tail, split_parts, kCtaRows, DV] unnormalised fp32 O
   float* split_ml;         // [split_tail, split_parts, kCtaRows, 2] row max (log2 units), row sum
+  // packed variable-length sequences (varlen != 0): q/o rows cu_q[b] .. cu_q[b+1] and k/v rows
+  // cu_k[b] .. cu_k[b+1] belong to sequence b; tile_prefix[b] counts the work tiles (2 x 128 query
+  // rows) of the sequences before b, tile_prefix[B] all of them; lse is [Hq, total_q]
+  int varlen, total_q;
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  const int32_t* tile_prefix;
+};
+
+struct VarlenPrepParams {
+  const int32_t* cu_q;     // [B + 1] query row offsets
+  const int32_t* cu_k;     // [B + 1] key row offsets
+  int B, total_q, total_k;
+  int max_tiles;           // work tiles the prefill launch has units for
+  int32_t* tile_prefix;    // [B + 1]
+  uint32_t* status;        // device status word
 };
 
 // Key-range split of the last, partial wave of work tiles.  With items work tiles on sms
@@ -133,5 +149,6 @@ cudaError_t device_status_ptr(uint32_t** out);
 bool encode_bshd(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int esize, int B, int S, int H, int Dh,
                  int64_t sb, int64_t ss, int64_t sh, int box0, int box_rows, CUtensorMapSwizzle sw);
 cudaError_t launch_mask_convert(const MaskConvertParams& p, cudaStream_t st);
+cudaError_t launch_varlen_prep(const VarlenPrepParams& p, cudaStream_t st);
 
 }  // namespace sdpa

@@ -130,7 +130,25 @@ struct WorkTile {
   int n_blocks;           // blocks streamed for the unit = max over its query tiles
   int jb0;                // first key block
   int split, part;        // split work tile and key range, or split = -1
+  int sq, sk;             // query and key rows of the sequence
+  int q_off, k_off, cb;   // TMA coordinates: first query / key row and batch index of the sequence
 };
+
+// Element offset of O row qrow of work tile w, and the index of its LSE entry.
+template <bool VARLEN>
+__device__ __forceinline__ int64_t o_offset(const PrefillParams& p, const WorkTile& w, int qrow) {
+  if constexpr (VARLEN)
+    return static_cast<int64_t>(w.q_off + qrow) * p.o_s + static_cast<int64_t>(w.h) * p.o_h;
+  else
+    return static_cast<int64_t>(w.b) * p.o_b + static_cast<int64_t>(qrow) * p.o_s + static_cast<int64_t>(w.h) * p.o_h;
+}
+template <bool VARLEN>
+__device__ __forceinline__ int64_t lse_index(const PrefillParams& p, const WorkTile& w, int qrow) {
+  if constexpr (VARLEN)
+    return static_cast<int64_t>(w.h) * p.total_q + w.q_off + qrow;
+  else
+    return (static_cast<int64_t>(w.b) * p.Hq + w.h) * p.Sq + qrow;
+}
 
 // Work tiles in launch order.  A KV unit is one (batch, KV head): its K/V are shared by the
 // Hq/Hkv query heads of the group and all their query tiles.  Units are taken in groups of
@@ -138,47 +156,80 @@ struct WorkTile {
 // K/V fits in L2), so the K/V that the CTAs running at the same time need stays resident in L2.
 // Inside a group, causal tiles at the bottom of the matrix see the most keys and come first;
 // tiles of one row band are ordered by unit, then query head.
-template <bool CAUSAL>
+template <bool CAUSAL, bool VARLEN>
 __device__ __forceinline__ WorkTile work_tile(const PrefillParams& p, int work_unit) {
   WorkTile w;
-  // work units past the whole work tiles are key ranges of the split tail (never causal)
-  int item = work_unit, parts = 1;
-  w.split = -1, w.part = 0;
-  if (!CAUSAL && work_unit >= p.n_full) {
-    const int r = work_unit - p.n_full;
-    parts = p.split_parts;
-    w.split = r / parts;
-    w.part = r - w.split * parts;
-    item = p.n_full + w.split;
+  w.split = -1, w.part = 0, w.jb0 = 0;
+  int jb1 = p.n_kblocks;
+  if constexpr (VARLEN) {
+    // unit = (tile of the packed sequences) * Hq + head; a sequence's tiles run longest first
+    // when causal.  Units past the last tile are empty.
+    const int total_tiles = __ldg(p.tile_prefix + p.B);
+    const int tg = work_unit / p.Hq;
+    w.h = work_unit - tg * p.Hq;
+    w.kvh = w.h / p.group;
+    if (tg >= total_tiles) {
+      w.b = 0, w.q0 = 0, w.sq = 0, w.sk = 0, w.q_off = 0, w.k_off = 0, w.cb = 0;
+      w.n_t[0] = w.n_t[1] = 0;
+      w.n_blocks = 0;
+      return w;
+    }
+    int lo = 0, hi = p.B;  // tile_prefix[lo] <= tg < tile_prefix[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(p.tile_prefix + mid) <= tg) lo = mid; else hi = mid;
+    }
+    const int first = __ldg(p.tile_prefix + lo), n_tiles = __ldg(p.tile_prefix + lo + 1) - first;
+    const int local = tg - first;
+    w.b = lo;
+    w.q0 = (CAUSAL ? n_tiles - 1 - local : local) * kCtaRows;
+    w.q_off = __ldg(p.cu_q + lo);
+    w.sq = __ldg(p.cu_q + lo + 1) - w.q_off;
+    w.k_off = __ldg(p.cu_k + lo);
+    w.sk = __ldg(p.cu_k + lo + 1) - w.k_off;
+    w.cb = 0;
+    // a sequence without keys still gets one (fully masked) block: its rows come out O = 0, LSE = -inf
+    jb1 = max(1, (w.sk + kBlockK - 1) / kBlockK);
+  } else {
+    // work units past the whole work tiles are key ranges of the split tail (never causal)
+    int item = work_unit, parts = 1;
+    if (!CAUSAL && work_unit >= p.n_full) {
+      const int r = work_unit - p.n_full;
+      parts = p.split_parts;
+      w.split = r / parts;
+      w.part = r - w.split * parts;
+      item = p.n_full + w.split;
+    }
+    w.jb0 = w.part * p.n_kblocks / parts;
+    jb1 = (w.part + 1) * p.n_kblocks / parts;
+    const int G = p.group;                           // query heads per KV head
+    const int units = p.B * p.Hkv;
+    const int per_unit = G * p.n_cta_tiles;          // work tiles of one KV unit
+    const int gsize = p.units_per_group * per_unit;  // work tiles of a full group
+    const int gi = item / gsize;
+    const int base = gi * p.units_per_group;
+    const int ul = min(p.units_per_group, units - base);  // units in this group (last may be short)
+    const int r = item - gi * gsize;
+    const int rank = r / (ul * G);                   // row band, longest first when causal
+    const int q = r - rank * (ul * G);
+    const int unit = base + q / G;
+    const int ctile = CAUSAL ? (p.n_cta_tiles - 1 - rank) : rank;
+    w.b = unit / p.Hkv;
+    w.kvh = unit % p.Hkv;
+    w.h = w.kvh * G + q % G;
+    w.q0 = ctile * kCtaRows;
+    w.sq = p.Sq, w.sk = p.Sk;
+    w.q_off = 0, w.k_off = 0, w.cb = w.b;
   }
-  const int jb0 = w.part * p.n_kblocks / parts;
-  const int jb1 = (w.part + 1) * p.n_kblocks / parts;
-  w.jb0 = jb0;
-  const int G = p.group;                           // query heads per KV head
-  const int units = p.B * p.Hkv;
-  const int per_unit = G * p.n_cta_tiles;          // work tiles of one KV unit
-  const int gsize = p.units_per_group * per_unit;  // work tiles of a full group
-  const int gi = item / gsize;
-  const int base = gi * p.units_per_group;
-  const int ul = min(p.units_per_group, units - base);  // units in this group (last may be short)
-  const int r = item - gi * gsize;
-  const int rank = r / (ul * G);                   // row band, longest first when causal
-  const int q = r - rank * (ul * G);
-  const int unit = base + q / G;
-  const int ctile = CAUSAL ? (p.n_cta_tiles - 1 - rank) : rank;
-  w.b = unit / p.Hkv;
-  w.kvh = unit % p.Hkv;
-  w.h = w.kvh * G + q % G;
-  w.q0 = ctile * kCtaRows;
   w.n_blocks = 0;
 #pragma unroll
   for (int t = 0; t < kTilesPerCta; ++t) {
     const int r0 = w.q0 + t * kBlockQ;
     int n = 0;
-    if (r0 < p.Sq) {
-      n = jb1 - jb0;
+    if (r0 < w.sq) {
+      n = jb1 - w.jb0;
       if (CAUSAL) {
-        const int last_row = min(r0 + kBlockQ - 1, p.Sq - 1);
+        const int last_row = min(r0 + kBlockQ - 1, w.sq - 1);
         n = min(n, last_row / kBlockK + 1);
       }
     }
@@ -213,7 +264,7 @@ __device__ __forceinline__ int nth_item(int k) {
 // A rescale of O_t needs no barrier of its own: the commit behind s_full[t] for block j also
 // covers the P_t V of block j-1, which the same thread issued earlier.
 //   o_empty[t]              : the epilogue has read O_t (the next work tile may overwrite it)
-template <int ELEM, int D, int DV, bool CAUSAL, bool MASK>
+template <int ELEM, int D, int DV, bool CAUSAL, bool MASK, bool VARLEN>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
@@ -286,7 +337,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       int g = 0;           // ring steps issued
       bool ok = true;
       for (int k = 0, item = nth_item(0); ok && item < n_items; item = nth_item(++k)) {
-        const WorkTile w = work_tile<CAUSAL>(p, item);
+        const WorkTile w = work_tile<CAUSAL, VARLEN>(p, item);
+        if (VARLEN && w.n_blocks == 0) continue;  // an empty unit (past the packed sequences' tiles)
         for (int t = 0; t < kTilesPerCta && ok; ++t) {
           if (w.n_t[t] == 0) continue;
           if (qn[t] > 0 && !mbar_wait(&q_empty[t], (qn[t] - 1) & 1, abort_flag, p.status)) {
@@ -296,7 +348,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           mbar_arrive_expect_tx(&q_full[t], C::Q_BYTES);
           for (int c = 0; c < C::NCH_D; ++c)
             tma_load_4d(sQ + t * C::Q_BYTES + c * kBlockQ * C::CHB, &tm_q, &q_full[t], c * C::CH, w.h,
-                        w.q0 + t * kBlockQ, w.b);
+                        w.q_off + w.q0 + t * kBlockQ, w.cb);
           ++qn[t];
         }
         if constexpr (ELEM == kE4M3) {
@@ -311,13 +363,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             mbar_arrive_expect_tx(&in_full[s], C::K_BYTES);
             for (int c = 0; c < C::NCH_D; ++c)
               tma_load_4d(sK + s * C::K_BYTES + c * kBlockK * C::CHB, &tm_k, &in_full[s], c * C::CH, w.kvh,
-                          (w.jb0 + j) * kBlockK, w.b);
+                          w.k_off + (w.jb0 + j) * kBlockK, w.cb);
             if (r > 0 && !mbar_wait(&v_free[s], (r - 1) & 1, abort_flag, p.status)) {
               ok = false;
               break;
             }
             mbar_arrive_expect_tx(&v_full[s], C::VRAW_BYTES);
-            tma_load_4d(sVraw + s * C::VRAW_BYTES, &tm_v, &v_full[s], 0, w.kvh, (w.jb0 + j) * kBlockK, w.b);
+            tma_load_4d(sVraw + s * C::VRAW_BYTES, &tm_v, &v_full[s], 0, w.kvh, w.k_off + (w.jb0 + j) * kBlockK,
+                        w.cb);
           }
         } else {
           // step j of the work tile brings K(j) and V(j-1)
@@ -333,12 +386,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             if (has_k) {
               for (int c = 0; c < C::NCH_D; ++c)
                 tma_load_4d(sK + s * C::K_BYTES + c * kBlockK * C::CHB, &tm_k, &in_full[s], c * C::CH, w.kvh,
-                            (w.jb0 + j) * kBlockK, w.b);
+                            w.k_off + (w.jb0 + j) * kBlockK, w.cb);
             }
             if (has_v) {
               for (int c = 0; c < C::NCH_V; ++c)
                 tma_load_4d(sV + s * C::V_BYTES + c * kBlockK * 128, &tm_v, &in_full[s], c * 64, w.kvh,
-                            (w.jb0 + j - 1) * kBlockK, w.b);
+                            w.k_off + (w.jb0 + j - 1) * kBlockK, w.cb);
             }
           }
         }
@@ -375,7 +428,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       int g = 0;            // ring steps consumed
       bool ok = true;
       for (int k = 0, item = nth_item(0); ok && item < n_items; item = nth_item(++k)) {
-        const WorkTile w = work_tile<CAUSAL>(p, item);
+        const WorkTile w = work_tile<CAUSAL, VARLEN>(p, item);
+        if (VARLEN && w.n_blocks == 0) continue;  // an empty unit: skipped by every role
         for (int t = 0; t < kTilesPerCta && ok; ++t)
           if (w.n_t[t] > 0) ok = mbar_wait(&q_full[t], qn[t] & 1, abort_flag, p.status);
         // Ring block of step j: e4m3 uses block g + j for K(j) and g + j - 1 for V(j-1); the
@@ -473,7 +527,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       int g = 0;
       bool ok = true;
       for (int k = 0, item = nth_item(0); ok && item < n_items; item = nth_item(++k)) {
-        const WorkTile w = work_tile<CAUSAL>(p, item);
+        const WorkTile w = work_tile<CAUSAL, VARLEN>(p, item);
         for (int j = 0; j < w.n_blocks; ++j, ++g) {
           const int s = g % ST, r = g / ST;
           if (!mbar_wait(&v_full[s], r & 1, abort_flag, p.status)) {
@@ -510,11 +564,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     int on = 0;  // work tiles finished (o_full phases)
     bool ok = true;
     for (int k = 0, item = nth_item(0); ok && item < n_items; item = nth_item(++k)) {
-      const WorkTile w = work_tile<CAUSAL>(p, item);
+      const WorkTile w = work_tile<CAUSAL, VARLEN>(p, item);
       const int n = w.n_t[t];
       if (n == 0) continue;
       const int qrow = w.q0 + t * kBlockQ + row;
-      const bool row_valid = qrow < p.Sq;
+      const bool row_valid = qrow < w.sq;
       float m_used = -INFINITY;
       float l = 0.f;
       const uint4* bits_row = nullptr;
@@ -561,9 +615,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
         // the causal diagonal and the ragged last block: hide keys past the row / past Sk
         const int k0 = (w.jb0 + j) * kBlockK;
-        const bool edge = (CAUSAL && (k0 + kBlockK - 1 > w.q0 + t * kBlockQ)) || (k0 + kBlockK > p.Sk);
+        const bool edge = (CAUSAL && (k0 + kBlockK - 1 > w.q0 + t * kBlockQ)) || (k0 + kBlockK > w.sk);
         if (edge) {
-          const int lim = (CAUSAL ? min(p.Sk, qrow + 1) : p.Sk) - k0;
+          const int lim = (CAUSAL ? min(w.sk, qrow + 1) : w.sk) - k0;
 #pragma unroll
           for (int c = 0; c < kBlockK; ++c)
             if (c >= lim) s[c] = -INFINITY;
@@ -575,7 +629,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 p.mask + static_cast<int64_t>(w.b) * p.mask_b + static_cast<int64_t>(qrow) * p.mask_i;
 #pragma unroll
             for (int c = 0; c < kBlockK; ++c) {
-              if (k0 + c < p.Sk) {
+              if (k0 + c < w.sk) {
                 const float mv = __half2float(__ushort_as_half(__ldg(mrow + k0 + c)));
                 s[c] += mv * p.inv_scale;
               }
@@ -658,10 +712,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       }
       ++on;
       tc_fence_after();
-      uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
-                      2 * (static_cast<int64_t>(w.b) * p.o_b + static_cast<int64_t>(qrow) * p.o_s +
-                           static_cast<int64_t>(w.h) * p.o_h);
-      float* lse_out = p.lse ? p.lse + (static_cast<int64_t>(w.b) * p.Hq + w.h) * p.Sq + qrow : nullptr;
+      uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) + 2 * o_offset<VARLEN>(p, w, qrow);
+      float* lse_out = p.lse ? p.lse + lse_index<VARLEN>(p, w, qrow) : nullptr;
       if (w.split >= 0) {
         // one key range of a split work tile: store this part's unnormalised O row, row max
         // and row sum for split_combine_kernel
@@ -734,9 +786,9 @@ __global__ void __launch_bounds__(128) split_combine_kernel(const PrefillParams 
   const int prow = static_cast<int>((idx / kChunks) % kCtaRows);
   const int split = static_cast<int>(idx / (static_cast<long long>(kChunks) * kCtaRows));
   const int P = p.split_parts;
-  const WorkTile w = work_tile<false>(p, p.n_full + split * P);
+  const WorkTile w = work_tile<false, false>(p, p.n_full + split * P);
   const int qrow = w.q0 + prow;
-  if (qrow >= p.Sq) return;
+  if (qrow >= w.sq) return;
   const size_t slot0 = static_cast<size_t>(split) * P * kCtaRows + prow;
   float m[kMaxSplitParts], l[kMaxSplitParts];
   float M = -INFINITY;
@@ -764,14 +816,12 @@ __global__ void __launch_bounds__(128) split_combine_kernel(const PrefillParams 
     }
   }
   const float inv = (L > 0.f) ? p.out_scale / L : 0.f;
-  uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
-                  2 * (static_cast<int64_t>(w.b) * p.o_b + static_cast<int64_t>(qrow) * p.o_s +
-                       static_cast<int64_t>(w.h) * p.o_h);
+  uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) + 2 * o_offset<false>(p, w, qrow);
   *reinterpret_cast<uint4*>(orow + chunk * 16) =
       make_uint4(pack_out<ELEM>(acc[0] * inv, acc[1] * inv), pack_out<ELEM>(acc[2] * inv, acc[3] * inv),
                  pack_out<ELEM>(acc[4] * inv, acc[5] * inv), pack_out<ELEM>(acc[6] * inv, acc[7] * inv));
   if (chunk == 0 && p.lse != nullptr)
-    p.lse[(static_cast<int64_t>(w.b) * p.Hq + w.h) * p.Sq + qrow] = (L > 0.f) ? (M + __log2f(L)) * kLn2 : -INFINITY;
+    p.lse[lse_index<false>(p, w, qrow)] = (L > 0.f) ? (M + __log2f(L)) * kLn2 : -INFINITY;
 }
 
 }  // namespace sdpa

@@ -1,4 +1,5 @@
-// Prefill instances for e4m3 inputs: (D, Dv) in {(64, 64), (128, 128), (192, 128)} x causal x mask.
+// Prefill instances for e4m3 inputs: (D, Dv) in {(64, 64), (128, 128), (192, 128)} x causal x
+// (mask, packed sequences or neither).
 #include "prefill_launch.cuh"
 
 namespace sdpa {

@@ -113,13 +113,64 @@ int sdpa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
  * MLA prefill path streams FP8 e4m3 K/V with D != Dv.)
  *
  * Supported head dims: (D, Dv) in {(64, 64), (128, 128), (192, 128)}.  q/k/v strides must be
- * multiples of 16 elements.  out_dtype: SDPA_BF16 or SDPA_F16.  Other arguments as in
- * sdpa_fwd.
+ * multiples of 16 elements.  out_dtype: SDPA_BF16.  Other arguments as in sdpa_fwd.
  */
 int sdpa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,
                  int Sk, int D, int Dv, const int64_t* strides, float scale, int causal, const void* mask,
                  const int64_t* mask_strides, void* workspace, size_t workspace_bytes, float descale_q,
                  float descale_k, float descale_v, sdpa_dtype out_dtype, void* stream);
+
+/* Number of int64 entries in the packed (varlen) prefill stride array. */
+#define SDPA_FWD_VARLEN_NSTRIDES 8
+
+/*
+ * sdpa_fwd_varlen_workspace_size -- bytes of device scratch sdpa_fwd_varlen /
+ * sdpa_fwd_varlen_fp8 need for B sequences: the per-sequence work-tile prefix,
+ * round_up((B + 1) * 4, 16).  0 for B < 1.
+ */
+size_t sdpa_fwd_varlen_workspace_size(int B);
+
+/*
+ * sdpa_fwd_varlen -- the prefill of sdpa_fwd over B sequences of different lengths packed
+ * back to back (page "Xe SDPA Forward Mainloop", section "SageV1 concrete instance": the
+ * run-time variant selects a variable-length template parameter).  Sequence b owns query
+ * rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and key/value rows cu_seqlens_k[b] ..
+ * cu_seqlens_k[b+1]-1; it attends to its own keys only, and causal masking is top-left
+ * aligned within each sequence (key j visible to query i iff j <= i, both counted from the
+ * sequence's first row).  A sequence with queries but no keys gets O = 0, LSE = -inf.
+ *
+ *   q    [total_q, Hq, D]     in_dtype         k [total_k, Hkv, D]   in_dtype
+ *   v    [total_k, Hkv, Dv]   in_dtype         o [total_q, Hq, Dv]   out_dtype (written
+ *                                               for the rows some sequence owns)
+ *   lse  [Hq, total_q] fp32 contiguous, natural log; may be NULL
+ *   cu_seqlens_q, cu_seqlens_k: DEVICE int32 [B + 1], 4-byte aligned, non-decreasing, first
+ *            entry >= 0, last entry <= total_q (total_k).  Read on the device: offsets that
+ *            break these rules make the call store nothing and raise a status that
+ *            sdpa_check_device_status() reports as SDPA_ERR_INVALID.
+ *   max_seqlen_q: >= every cu_seqlens_q[b+1] - cu_seqlens_q[b] and <= total_q (it sizes
+ *            the launch; a longer sequence is reported like bad offsets).
+ *   strides: NULL for the contiguous layouts above, else 8 element strides
+ *            {q_s, q_h,  k_s, k_h,  v_s, v_h,  o_s, o_h} (row and head; head dim stride 1)
+ *   workspace: device scratch of sdpa_fwd_varlen_workspace_size(B) bytes, 16-byte aligned;
+ *            required.  Calls that overlap on the GPU need separate workspaces.
+ *   scale, causal, head dims, dtypes, alignment and stride rules: as in sdpa_fwd.
+ * No additive mask; B, Hq, Hkv, total_q, total_k, max_seqlen_q >= 1.  Two kernels run in
+ * `stream`: a one-block scan of the per-sequence tile counts, then the prefill.
+ */
+int sdpa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int32_t* cu_seqlens_q,
+                    const int32_t* cu_seqlens_k, int B, int Hq, int Hkv, int total_q, int total_k, int max_seqlen_q,
+                    int D, int Dv, const int64_t* strides, float scale, int causal, void* workspace,
+                    size_t workspace_bytes, sdpa_dtype in_dtype, sdpa_dtype out_dtype, void* stream);
+
+/*
+ * sdpa_fwd_varlen_fp8 -- sdpa_fwd_varlen with FP8 e4m3 Q/K/V codes and per-tensor scales,
+ * computed as in sdpa_fwd_fp8.  out_dtype: SDPA_BF16.
+ */
+int sdpa_fwd_varlen_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
+                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int B, int Hq, int Hkv, int total_q,
+                        int total_k, int max_seqlen_q, int D, int Dv, const int64_t* strides, float scale, int causal,
+                        void* workspace, size_t workspace_bytes, float descale_q, float descale_k, float descale_v,
+                        sdpa_dtype out_dtype, void* stream);
 
 /*
  * sdpa_decode_workspace_size -- bytes of device scratch sdpa_decode needs for per-split
@@ -204,8 +255,9 @@ int sdpa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
 /*
  * sdpa_check_device_status -- synchronizes `stream`, then reports and clears the device
  * status word the kernels raise when a bounded wait inside them gives up (a pipeline
- * stage that never arrived): SDPA_ERR_TIMEOUT in that case, SDPA_ERR_CUDA if the
- * synchronization itself failed, else SDPA_OK.  The status word is per device and per
+ * stage that never arrived): SDPA_ERR_TIMEOUT in that case, SDPA_ERR_INVALID when a varlen
+ * call found bad sequence offsets, SDPA_ERR_CUDA if the synchronization itself failed, else
+ * SDPA_OK.  The status word is per device and per
  * process, shared by all streams.
  */
 int sdpa_check_device_status(void* stream);

@@ -105,6 +105,60 @@ def sdpa_fwd(q, k, v, mask=None, *, scale: float, causal: bool = False, rows=Non
     return o, lse
 
 
+def _offsets(cu):
+    return [int(x) for x in (cu.tolist() if hasattr(cu, "tolist") else cu)]
+
+
+def sdpa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, *, scale: float, causal: bool = False, rows=None,
+                    descale=(1.0, 1.0, 1.0), nthreads: int | None = None):
+    """O and LSE of packed variable-length sequences in fp64.
+
+    q [total_q,Hq,D], k [total_k,Hkv,D], v [total_k,Hkv,Dv]; sequence b owns query rows
+    cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and key rows cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1.
+    Each sequence is its own attention problem (page "Xe SDPA Forward Mainloop", section "SageV1
+    concrete instance": the variable-length variant of the same mainloop), computed by sdpa_fwd
+    on its rows with causal masking counted from the sequence's first row.  A sequence with
+    queries but no keys has every score masked: O = 0, LSE = -inf (the fully-masked-row
+    convention of sdpa_fwd).
+
+    rows: optional int array [n, 2] of (packed query row, query head), each row owned by some
+    sequence; then O is [n, Dv] and LSE [n].  Otherwise O is [total_q, Hq, Dv] and LSE
+    [Hq, total_q], NaN on rows no sequence owns."""
+    cq, ck = _offsets(cu_seqlens_q), _offsets(cu_seqlens_k)
+    assert len(cq) == len(ck) >= 2
+    B = len(cq) - 1
+    total_q, Hq, _ = q.shape
+    Dv = v.shape[-1]
+
+    def seq(b, sel=None):
+        q0, q1, k0, k1 = cq[b], cq[b + 1], ck[b], ck[b + 1]
+        n = (q1 - q0) if sel is None else len(sel)
+        if k1 <= k0:
+            return np.zeros((n, Hq, Dv) if sel is None else (n, Dv)), np.full((Hq, n) if sel is None else (n,), -np.inf)
+        r = None if sel is None else np.array([(0, h, i) for (i, h) in sel], dtype=np.int64)
+        o, lse = sdpa_fwd(q[q0:q1][None], k[k0:k1][None], v[k0:k1][None], scale=scale, causal=causal, rows=r,
+                          descale=descale, nthreads=nthreads)
+        return (o[0], lse[0]) if sel is None else (o, lse)
+
+    if rows is None:
+        o = np.full((total_q, Hq, Dv), np.nan)
+        lse = np.full((Hq, total_q), np.nan)
+        for b in range(B):
+            if cq[b + 1] > cq[b]:
+                o[cq[b]:cq[b + 1]], lse[:, cq[b]:cq[b + 1]] = seq(b)
+        return o, lse
+    r = np.asarray(rows, dtype=np.int64).reshape(-1, 2)
+    owner = np.searchsorted(np.asarray(cq), r[:, 0], side="right") - 1
+    assert ((owner >= 0) & (owner < B)).all() and (r[:, 0] < cq[-1]).all(), "row owned by no sequence"
+    o = np.empty((len(r), Dv))
+    lse = np.empty((len(r),))
+    for b in np.unique(owner):
+        idx = np.nonzero(owner == b)[0]
+        ob, lb = seq(int(b), [(int(r[n, 0]) - cq[b], int(r[n, 1])) for n in idx])
+        o[idx], lse[idx] = ob, lb
+    return o, lse
+
+
 def sdpa_decode(q, k_cache, v_cache, kv_len, *, scale: float, batches=None, nthreads: int | None = None):
     """Decode oracle: q [B,Hq,D], caches [B,max_kv,Hkv,.], kv_len [B].
 

@@ -295,3 +295,66 @@ def test_workload_inputs_are_seeded_and_exact():
     assert int(full[0].sum()) >= 5 and int(full[1].sum()) >= 5
     frac = float(torch.isinf(m[~full]).float().mean())
     assert 0.08 < frac < 0.12
+
+
+def _block_diagonal_mask(cq, ck, causal):
+    """Additive [total_q, total_k] mask: 0 where query row i and key row j belong to the same
+    sequence (and, when causal, j's position in it is at most i's), else -inf."""
+    tq, tk = cq[-1], ck[-1]
+    m = torch.full((tq, tk), NEG_INF, dtype=torch.float64)
+    for b in range(len(cq) - 1):
+        nq, nk = cq[b + 1] - cq[b], ck[b + 1] - ck[b]
+        keep = torch.ones(nq, nk, dtype=torch.bool)
+        if causal:
+            keep = keep.tril()
+        m[cq[b]:cq[b + 1], ck[b]:ck[b + 1]] = torch.where(keep, 0.0, NEG_INF)
+    return m
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_equals_one_problem_with_block_diagonal_mask(causal):
+    # packed sequences are one attention problem over all rows whose mask confines every query to
+    # its own sequence's keys; torch's fp64 SDPA evaluates that problem independently of the oracle
+    seq_q, seq_k = [5, 0, 17, 1, 9, 3], [7, 4, 17, 1, 2, 0]
+    cq = [0, *np.cumsum(seq_q).tolist()]
+    ck = [0, *np.cumsum(seq_k).tolist()]
+    Hq, Hkv, D, Dv = 4, 2, 8, 6
+    q, k, v = _rand((cq[-1], Hq, D), 41), _rand((ck[-1], Hkv, D), 42), _rand((ck[-1], Hkv, Dv), 43)
+    o, lse = oracle.sdpa_fwd_varlen(q, k, v, cq, ck, scale=0.7, causal=causal)
+    mask = _block_diagonal_mask(cq, ck, causal)
+    ref = _torch_sdpa(q[None], k[None], v[None], mask[None], 0.7, False)[0].numpy()
+    ref_lse = _torch_lse(q[None], k[None], mask[None], 0.7, False)[0].numpy()
+    empty = np.isneginf(ref_lse[0])  # query rows of the sequence without keys
+    assert empty.sum() == seq_q[5]
+    assert np.abs(o[~empty] - ref[~empty]).max() <= 1e-12
+    assert np.abs(lse[:, ~empty] - ref_lse[:, ~empty]).max() <= 1e-12
+    assert (o[empty] == 0.0).all() and np.isneginf(lse[:, empty]).all()
+
+
+def test_varlen_equal_lengths_is_the_dense_batch():
+    B, S, Hq, Hkv, D, Dv = 3, 21, 4, 4, 16, 16
+    q, k, v = _rand((B, S, Hq, D), 44), _rand((B, S, Hkv, D), 45), _rand((B, S, Hkv, Dv), 46)
+    cu = [b * S for b in range(B + 1)]
+    o, lse = oracle.sdpa_fwd_varlen(q.reshape(B * S, Hq, D), k.reshape(B * S, Hkv, D), v.reshape(B * S, Hkv, Dv),
+                                    cu, cu, scale=0.5, causal=True)
+    ref_o, ref_lse = oracle.sdpa_fwd(q, k, v, scale=0.5, causal=True)
+    assert np.array_equal(o, ref_o.reshape(B * S, Hq, Dv))
+    assert np.array_equal(lse, ref_lse.transpose(1, 0, 2).reshape(Hq, B * S))
+
+
+def test_varlen_rows_and_unowned_rows():
+    seq = [4, 0, 6]
+    x = workloads.varlen_pack(seq, seq, 2, 1, 8, 8, dtype="bf16", seed=3, pad_q=2, pad_k=1)
+    o, lse = oracle.sdpa_fwd_varlen(x["q"], x["k"], x["v"], x["cu_q"], x["cu_k"], scale=0.3, causal=True)
+    assert np.isnan(o[10:]).all() and np.isnan(lse[:, 10:]).all()  # padding rows belong to no sequence
+    assert not np.isnan(o[:10]).any()
+    # causal: the first row of each sequence is its first V row
+    v = oracle.as_f64(x["v"])
+    assert np.array_equal(o[0, 1], v[0, 0]) and np.array_equal(o[4, 0], v[4, 0])
+    rows = np.array([[9, 1], [0, 0], [5, 1], [3, 0]])
+    os_, ls = oracle.sdpa_fwd_varlen(x["q"], x["k"], x["v"], x["cu_q"], x["cu_k"], scale=0.3, causal=True,
+                                     rows=rows)
+    for n, (i, h) in enumerate(rows):
+        assert np.array_equal(os_[n], o[i, h]) and ls[n] == lse[h, i]
+    with pytest.raises(AssertionError):
+        oracle.sdpa_fwd_varlen(x["q"], x["k"], x["v"], x["cu_q"], x["cu_k"], scale=0.3, rows=[[10, 0]])

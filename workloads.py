@@ -72,6 +72,10 @@ WORKLOADS = {
                  dtype="bf16", dist="normal", out_dtype="bf16", kv_len_range=(1024, 16384)),
         Workload("mla_fp8_causal_prefill_d192", 5, "prefill", B=1, Hq=128, Hkv=128, Sq=8192, Sk=8192, D=192,
                  Dv=128, dtype="e4m3", dist="normal", causal=True, out_dtype="bf16"),
+        # packed sequences: B sequence lengths drawn uniformly from len_range, keys = queries
+        Workload("varlen_causal_prefill_bf16_d128", 6, "varlen", B=16, Hq=32, Hkv=8, Sq=8192, Sk=8192, D=128,
+                 Dv=128, dtype="bf16", dist="normal", causal=True, out_dtype="bf16",
+                 extra={"len_range": (64, 8192)}),
     ]
 }
 
@@ -194,3 +198,37 @@ def custom_prefill(B, Hq, Hkv, Sq, Sk, D, Dv, dtype="bf16", dist="normal", seed=
     v, sv = _store(_draw(g, (B, Sk, Hkv, Dv), dist), dtype)
     m = make_mask(g, B, Sq, Sk, masked_frac, full_row_frac) if mask else None
     return {"q": q, "k": k, "v": v, "mask": m, "descale": (sq, sk, sv)}
+
+
+def varlen_pack(seq_q, seq_k, Hq, Hkv, D, Dv, dtype="bf16", dist="normal", seed=0, pad_q=0, pad_k=0):
+    """Packed sequences: q [total_q, Hq, D], k [total_k, Hkv, D], v [total_k, Hkv, Dv] with sequence b
+    on rows cu_q[b] .. cu_q[b+1] (keys likewise), cu_q / cu_k int32 [B + 1].  ``pad_q`` / ``pad_k``
+    extra rows at the end belong to no sequence.  Draw order: q, k, v over all rows (e4m3: one
+    per-tensor scale each)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    cu_q = torch.zeros(len(seq_q) + 1, dtype=torch.int32)
+    cu_k = torch.zeros(len(seq_k) + 1, dtype=torch.int32)
+    cu_q[1:] = torch.cumsum(torch.as_tensor(seq_q, dtype=torch.int64), 0).to(torch.int32)
+    cu_k[1:] = torch.cumsum(torch.as_tensor(seq_k, dtype=torch.int64), 0).to(torch.int32)
+    tq, tk = int(cu_q[-1]) + pad_q, int(cu_k[-1]) + pad_k
+    q, sq = _store(_draw(g, (tq, Hq, D), dist), dtype)
+    k, sk = _store(_draw(g, (tk, Hkv, D), dist), dtype)
+    v, sv = _store(_draw(g, (tk, Hkv, Dv), dist), dtype)
+    return {"q": q, "k": k, "v": v, "cu_q": cu_q, "cu_k": cu_k, "descale": (sq, sk, sv)}
+
+
+def varlen_lengths(w: Workload, rotation: int = 0):
+    """Sequence lengths of a packed workload: B draws, uniform over the inclusive len_range."""
+    lo, hi = w.extra["len_range"]
+    g = generator(w.index, rotation)
+    return [int(x) for x in torch.randint(lo, hi + 1, (w.B,), generator=g, dtype=torch.int64)]
+
+
+def varlen_inputs(w: Workload, rotation: int = 0):
+    """Packed inputs of a varlen workload (query and key lengths equal)."""
+    assert w.kind == "varlen"
+    lens = varlen_lengths(w, rotation)
+    x = varlen_pack(lens, lens, w.Hq, w.Hkv, w.D, w.Dv, w.dtype, w.dist, seed=1000 * w.index + rotation + 500)
+    x["lengths"] = lens
+    return x
