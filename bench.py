@@ -267,6 +267,39 @@ def bench_varlen(w, K, W, dev, peaks, flusher):
                          "peak_note": "bf16 burst, of " + peaks["source"], "traffic": recorded_traffic(w.name)}}
 
 
+def int8_setup(w, dev, rotation=0):
+    import flash_attention_forward_gb300 as fa
+
+    x = workloads.int8_inputs(w, rotation)
+    g = {n: (None if t is None else t.to(dev)) for n, t in x.items()}
+    out_dtype = workloads.torch_dtype(w.out_dtype)
+    o = torch.empty((w.B, w.Sq, w.Hq, w.Dv), dtype=out_dtype, device=dev)
+    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+    ws = torch.empty(fa.sdpa_fwd_int8_workspace_size(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, g["v_scale"] is not None,
+                                                     w.causal), dtype=torch.uint8, device=dev)
+
+    def step(_i=0):
+        fa.sdpa_fwd_int8(g["q"], g["k"], g["v"], g["q_scale"], g["k_scale"], g["v_scale"], scale=w.scale,
+                         causal=w.causal, out_dtype=out_dtype, out=o, lse=lse, workspace=ws)
+
+    return x, step
+
+
+def bench_int8(w, K, W, dev, peaks, flusher):
+    """int8 Q/K codes: the widening copy and the block-scaled prefill per step."""
+    _, step = int8_setup(w, dev)
+    ms = time_steps(step, K, W, flusher)
+    flops = prefill_flops(w)
+    avg = sum(ms) / len(ms)
+    tflops = flops / (avg * 1e-3) / 1e12
+    bf16 = peaks["bf16_tflops"]
+    return {"workload": w.name, "value": tflops, "unit": "TFLOP/s", "ms_per_step": avg, "flops_per_step": flops,
+            "launches_per_step": 2,
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": bf16, "unit": "TFLOP/s", "frac": tflops / bf16,
+                         "peak_note": "16-bit MMA (no int8 MMA on sm_103a); bf16 burst, of " + peaks["source"],
+                         "traffic": recorded_traffic(w.name)}}
+
+
 def bench_decode(w, K, W, dev, peaks, page_size: int = 64):
     """The split-KV decode over 4 rotating input sets (each far larger than L2), then the same
     rows in page_size-row pages scattered over a pool (the paged decode).  Returns both lines."""
@@ -487,6 +520,8 @@ def profile_run(args):
                 fa.sdpa_decode(q, k, v, kvl, scale=w.scale, workspace=ws)
     elif w.kind == "varlen":
         _, step = varlen_setup(w, dev)
+    elif w.dtype == "i8":
+        _, step = int8_setup(w, dev)
     else:
         _, step = prefill_setup(w, dev)
     ms = time_steps(step, max(args.steps, 1), max(args.warmup, 1))
@@ -558,6 +593,9 @@ def main():
         for name in ("tiny_prefill_f16_d64", "unaligned_mask_prefill_bf16_d128", "mla_fp8_causal_prefill_d192"):
             others[name] = bench_prefill(workloads.WORKLOADS[name], k2, args.warmup, dev, peaks, flusher)
             torch.cuda.empty_cache()
+        iw = workloads.WORKLOADS["int8_qk_causal_prefill_d128"]
+        others[iw.name] = bench_int8(iw, k2, args.warmup, dev, peaks, flusher)
+        torch.cuda.empty_cache()
         vw = workloads.WORKLOADS["varlen_causal_prefill_bf16_d128"]
         others[vw.name] = bench_varlen(vw, k2, args.warmup, dev, peaks, flusher)
         torch.cuda.empty_cache()

@@ -12,10 +12,12 @@ Entry points (same names as the C ABI):
     sdpa_fwd_fp8(q, k, v, dq, dk, dv, ...)     e4m3 prefill with per-tensor scales
     sdpa_fwd_varlen(q, k, v, cu_q, cu_k, max_seqlen_q, ...)   prefill of packed sequences
     sdpa_fwd_varlen_fp8(q, k, v, cu_q, cu_k, max_seqlen_q, dq, dk, dv, ...)   the same in e4m3
+    sdpa_fwd_int8(q, k, v, q_scale, k_scale, v_scale, ...)   int8 Q/K codes with per-block scales
     sdpa_decode(q, k_cache, v_cache, kv_len, ...)   two-phase split-KV decode
     sdpa_decode_paged(q, k_pool, v_pool, page_table, kv_len, ...)   the same over a paged cache
     sdpa_decode_noalloc(q, k_cache, v_cache, kv_len, ...)   the same with library-owned scratch
-    sdpa_fwd_workspace_size, sdpa_fwd_varlen_workspace_size, sdpa_decode_workspace_size,
+    sdpa_fwd_workspace_size, sdpa_fwd_varlen_workspace_size, sdpa_fwd_int8_workspace_size,
+    sdpa_decode_workspace_size,
     sdpa_check_device_status,
     sdpa_status_string, sdpa_version
 """
@@ -34,8 +36,8 @@ LIB_PATH = os.path.join(_HERE, "libsdpa_gb300.so")
 HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "sdpa.h")
 
 SDPA_OK, SDPA_ERR_INVALID, SDPA_ERR_UNSUPPORTED, SDPA_ERR_CUDA, SDPA_ERR_TIMEOUT = range(5)
-SDPA_F16, SDPA_BF16, SDPA_E4M3 = range(3)
-_DT = {torch.float16: SDPA_F16, torch.bfloat16: SDPA_BF16, torch.float8_e4m3fn: SDPA_E4M3}
+SDPA_F16, SDPA_BF16, SDPA_E4M3, SDPA_I8 = range(4)
+_DT = {torch.float16: SDPA_F16, torch.bfloat16: SDPA_BF16, torch.float8_e4m3fn: SDPA_E4M3, torch.int8: SDPA_I8}
 
 _lock = threading.Lock()
 _lib = None
@@ -70,6 +72,10 @@ def _load():
         lib.sdpa_fwd_varlen_fp8.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, i, i, i, p, f, i, p, sz, f, f, f, i,
                                             p]
         lib.sdpa_fwd_varlen_fp8.restype = i
+        lib.sdpa_fwd_int8_workspace_size.argtypes = [i, i, i, i, i, i, i, i]
+        lib.sdpa_fwd_int8_workspace_size.restype = sz
+        lib.sdpa_fwd_int8.argtypes = [p, p, p, p, p, i, i, i, i, i, i, p, p, p, p, f, i, p, sz, i, i, p]
+        lib.sdpa_fwd_int8.restype = i
         lib.sdpa_decode_workspace_size.argtypes = [i, i, i, i]
         lib.sdpa_decode_workspace_size.restype = sz
         lib.sdpa_decode.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, p, f, p, sz, i, p]
@@ -262,6 +268,54 @@ def sdpa_fwd_varlen_fp8(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, 
                                      strides, scale, int(bool(causal)), _ptr(workspace), ws_bytes, float(descale_q),
                                      float(descale_k), float(descale_v), _DT[out.dtype], _stream_ptr(stream))
     _check("sdpa_fwd_varlen_fp8", rc)
+    return out, lse
+
+
+def sdpa_fwd_int8_workspace_size(B: int, Hq: int, Hkv: int, Sq: int, Sk: int, D: int, v_int8: bool,
+                                 causal: bool) -> int:
+    """Bytes of workspace for sdpa_fwd_int8: 16-bit copies of the int8 operands, then the optional
+    split partials."""
+    return int(_load().sdpa_fwd_int8_workspace_size(B, Hq, Hkv, Sq, Sk, D, int(bool(v_int8)), int(bool(causal))))
+
+
+def sdpa_fwd_int8(q, k, v, q_scale, k_scale, v_scale=None, *, scale: float | None = None, causal: bool = False,
+                  out_dtype=torch.float16, out=None, lse=None, return_lse: bool = True, workspace=None,
+                  stream=None):
+    """Prefill with int8 codes: q [B,Sq,Hq,D], k [B,Sk,Hkv,D] int8 with fp32 scales q_scale
+    [B,Hq,ceil(Sq/128)], k_scale [B,Hkv,ceil(Sk/128)] (one per 128-row block); v either out_dtype values
+    or int8 codes with per-channel v_scale [B,Hkv,D].  Returns (o [B,Sq,Hq,D] out_dtype, lse or None)."""
+    if q.dtype != torch.int8 or k.dtype != torch.int8:
+        raise ValueError("sdpa_fwd_int8 takes int8 q and k codes")
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, S, H, D]")
+    B, Sq, Hq, D = q.shape
+    _, Sk, Hkv, _ = k.shape
+    for t in (q, k, v):
+        if not t.is_cuda or t.stride(-1) != 1:
+            raise ValueError("q, k, v must be CUDA tensors with unit innermost stride")
+    nqb, nkb = (Sq + 127) // 128, (Sk + 127) // 128
+    checks = [(q_scale, (B, Hq, nqb), "q_scale"), (k_scale, (B, Hkv, nkb), "k_scale")]
+    if v_scale is not None:
+        checks.append((v_scale, (B, Hkv, D), "v_scale"))
+    for t, shape, name in checks:
+        if t.dtype != torch.float32 or not t.is_cuda or tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous fp32 CUDA tensor of shape {shape}")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty((B, Sq, Hq, D), dtype=out_dtype, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    if lse is not None and (tuple(lse.shape) != (B, Hq, Sq) or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous fp32 [B, Hq, Sq] tensor")
+    if workspace is None:
+        workspace = torch.empty(max(16, sdpa_fwd_int8_workspace_size(B, Hq, Hkv, Sq, Sk, D, v.dtype == torch.int8,
+                                                                     causal)), dtype=torch.uint8, device=q.device)
+    strides = _i64([*q.stride()[:3], *k.stride()[:3], *v.stride()[:3], *out.stride()[:3]])
+    rc = _load().sdpa_fwd_int8(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk, D, strides,
+                               _ptr(q_scale), _ptr(k_scale), _ptr(v_scale), scale, int(bool(causal)),
+                               _ptr(workspace), workspace.numel() * workspace.element_size(), _DT[v.dtype],
+                               _DT[out.dtype], _stream_ptr(stream))
+    _check("sdpa_fwd_int8", rc)
     return out, lse
 
 

@@ -17,7 +17,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_obj")
 LIB = os.path.join(HERE, "libsdpa_gb300.so")
-SOURCES = ["api.cu", "decode.cu", "prefill_f16.cu", "prefill_bf16.cu", "prefill_e4m3.cu", "decode_noalloc.cu"]
+SOURCES = ["api.cu", "decode.cu", "prefill_f16.cu", "prefill_bf16.cu", "prefill_e4m3.cu", "decode_noalloc.cu",
+           "widen.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-I" + os.path.join(ROOT, "include")]

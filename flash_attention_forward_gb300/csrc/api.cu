@@ -117,13 +117,22 @@ long long varlen_max_tiles(int B, int total_q, int max_seqlen_q) {
   return by_max < by_total ? by_max : by_total;
 }
 
-// Shared body of the dense and packed entry points (vl != null: B sequences packed as
-// described by *vl; Sq, Sk are then the longest query length and total_k).
+// int8 codes: per-block scales, and the widening of the codes that runs just before the prefill.
+struct Int8Args {
+  const float* q_scale;
+  const float* k_scale;
+  const float* v_scale;
+  WidenParams widen;
+};
+
+// Shared body of the dense, packed and int8-code entry points (vl != null: B sequences packed as
+// described by *vl; Sq, Sk are then the longest query length and total_k.  i8 != null: q, k (and
+// v) are the 16-bit copies that i8->widen writes, scaled per block).
 int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,
                int Sk, int D, int Dv, const int64_t* strides, float scale, int causal, const void* mask,
                const int64_t* mask_strides, void* workspace, size_t workspace_bytes, int elem, float descale_q,
                float descale_k, float descale_v, sdpa_dtype out_dtype, void* stream,
-               const VarlenArgs* vl = nullptr) {
+               const VarlenArgs* vl = nullptr, const Int8Args* i8 = nullptr) {
   // ---- validation (no CUDA call before this block passes)
   if (!q || !k || !v || !o) return SDPA_ERR_INVALID;
   if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Sk < 1 || D < 1 || Dv < 1) return SDPA_ERR_INVALID;
@@ -174,6 +183,7 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   const long long n_items = vl ? varlen_max_tiles(B, vl->total_q, vl->max_seqlen_q) * Hq
                                : (long long)n_cta_tiles * B * Hq;
   if (n_items * kMaxSplitParts >= (1ll << 31)) return SDPA_ERR_UNSUPPORTED;
+  if (i8 && (mask || vl || elem == kE4M3 || D != Dv || D == 192)) return SDPA_ERR_UNSUPPORTED;
   if (vl) {
     if (!vl->cu_q || !vl->cu_k || mask) return SDPA_ERR_INVALID;
     if ((reinterpret_cast<uintptr_t>(vl->cu_q) | reinterpret_cast<uintptr_t>(vl->cu_k)) & 3u) return SDPA_ERR_INVALID;
@@ -262,6 +272,17 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   }
   bool supported = false;
   cudaError_t e;
+  if (i8) {
+    if (launch_widen(i8->widen, stm) != cudaSuccess) return SDPA_ERR_CUDA;
+    p.q_scale = i8->q_scale;
+    p.k_scale = i8->k_scale;
+    p.v_scale = i8->v_scale;
+    p.n_qblocks = (Sq + kBlockQ - 1) / kBlockQ;
+    e = elem == kBF16 ? launch_prefill_bf16_block_scaled(D, causal != 0, tq, tk, tv, p, stm, &supported)
+                      : launch_prefill_f16_block_scaled(D, causal != 0, tq, tk, tv, p, stm, &supported);
+    if (!supported) return SDPA_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+  }
   if (elem == kE4M3)
     e = launch_prefill_e4m3(D, Dv, causal != 0, mask != nullptr, tq, tk, tv, p, stm, &supported);
   else if (elem == kBF16)
@@ -337,6 +358,79 @@ int sdpa_fwd_varlen_fp8(const void* q, const void* k, const void* v, void* o, fl
   return fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv, total_q, total_k, max_seqlen_q, D, Dv,
                     strides, scale, causal, workspace, workspace_bytes, kE4M3, descale_q, descale_k, descale_v,
                     out_dtype, stream);
+}
+
+namespace {
+// Bytes of the widened 16-bit copies of the int8 operands (Q, K, and V when it is int8).
+size_t int8_widened_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, bool v_int8) {
+  const size_t q = round16((size_t)B * Sq * Hq * D * 2), kv = round16((size_t)B * Sk * Hkv * D * 2);
+  return q + kv + (v_int8 ? kv : 0);
+}
+}  // namespace
+
+size_t sdpa_fwd_int8_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, int v_int8, int causal) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Sk < 1 || D < 1) return 0;
+  return int8_widened_bytes(B, Hq, Hkv, Sq, Sk, D, v_int8 != 0) +
+         prefill_split_bytes(fwd_split_plan(B, Hq, Sq, Sk, causal != 0), D);
+}
+
+int sdpa_fwd_int8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,
+                  int Sk, int D, const int64_t* strides, const float* q_scale, const float* k_scale,
+                  const float* v_scale, float scale, int causal, void* workspace, size_t workspace_bytes,
+                  sdpa_dtype v_dtype, sdpa_dtype out_dtype, void* stream) {
+  if (!q || !k || !v || !o || !q_scale || !k_scale) return SDPA_ERR_INVALID;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Sk < 1 || D < 1) return SDPA_ERR_INVALID;
+  if (out_dtype != SDPA_F16 && out_dtype != SDPA_BF16) return SDPA_ERR_UNSUPPORTED;
+  if (v_dtype != SDPA_I8 && v_dtype != out_dtype) return SDPA_ERR_UNSUPPORTED;
+  const bool v_int8 = v_dtype == SDPA_I8;
+  if (v_int8 != (v_scale != nullptr)) return SDPA_ERR_INVALID;
+  if (D != 64 && D != 128) return SDPA_ERR_UNSUPPORTED;
+  if (((reinterpret_cast<uintptr_t>(q_scale) | reinterpret_cast<uintptr_t>(k_scale)) & 3u) ||
+      (v_scale && !aligned16(v_scale)))
+    return SDPA_ERR_INVALID;
+  int64_t st[SDPA_FWD_NSTRIDES];
+  if (strides) {
+    std::memcpy(st, strides, sizeof(st));
+  } else {
+    const int64_t cs[SDPA_FWD_NSTRIDES] = {(int64_t)Sq * Hq * D, (int64_t)Hq * D, D, (int64_t)Sk * Hkv * D,
+                                           (int64_t)Hkv * D,     D,               (int64_t)Sk * Hkv * D,
+                                           (int64_t)Hkv * D,     D,               (int64_t)Sq * Hq * D,
+                                           (int64_t)Hq * D,      D};
+    std::memcpy(st, cs, sizeof(st));
+  }
+  // int8 operands: 16-byte rows for the widening loads
+  for (int i = 0; i < (v_int8 ? 9 : 6); ++i)
+    if (!stride_ok(st[i], 16)) return SDPA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || (v_int8 && !aligned16(v))) return SDPA_ERR_UNSUPPORTED;
+  const size_t wide = int8_widened_bytes(B, Hq, Hkv, Sq, Sk, D, v_int8);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < wide) return SDPA_ERR_INVALID;
+
+  char* ws = static_cast<char*>(workspace);
+  void* q16 = ws;
+  void* k16 = ws + round16((size_t)B * Sq * Hq * D * 2);
+  void* v16 = v_int8 ? static_cast<char*>(k16) + round16((size_t)B * Sk * Hkv * D * 2) : const_cast<void*>(v);
+  Int8Args a{q_scale, k_scale, v_scale, WidenParams{}};
+  a.widen.to_bf16 = out_dtype == SDPA_BF16;
+  a.widen.seg[0] = WidenSeg{static_cast<const int8_t*>(q), st[0], st[1], st[2], B, Sq, Hq, D, q16};
+  a.widen.seg[1] = WidenSeg{static_cast<const int8_t*>(k), st[3], st[4], st[5], B, Sk, Hkv, D, k16};
+  if (v_int8) a.widen.seg[2] = WidenSeg{static_cast<const int8_t*>(v), st[6], st[7], st[8], B, Sk, Hkv, D, v16};
+  a.widen.n_seg = v_int8 ? 3 : 2;
+  // the prefill reads the contiguous copies; V keeps the caller's strides when it is 16-bit
+  const int64_t st16[SDPA_FWD_NSTRIDES] = {(int64_t)Sq * Hq * D,
+                                           (int64_t)Hq * D,
+                                           D,
+                                           (int64_t)Sk * Hkv * D,
+                                           (int64_t)Hkv * D,
+                                           D,
+                                           v_int8 ? (int64_t)Sk * Hkv * D : st[6],
+                                           v_int8 ? (int64_t)Hkv * D : st[7],
+                                           v_int8 ? (int64_t)D : st[8],
+                                           st[9],
+                                           st[10],
+                                           st[11]};
+  return fwd_common(q16, k16, v16, o, lse, B, Hq, Hkv, Sq, Sk, D, D, st16, scale, causal, nullptr, nullptr,
+                    ws + wide, workspace_bytes - wide, out_dtype == SDPA_BF16 ? kBF16 : kF16, 1.f, 1.f, 1.f,
+                    out_dtype, stream, nullptr, &a);
 }
 
 size_t sdpa_decode_workspace_size(int B, int Hq, int max_kv, int Dv) {

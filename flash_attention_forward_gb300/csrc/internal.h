@@ -22,6 +22,11 @@ constexpr int kPrefillThreads = 384;   // 12 warps: load, MMA, 2 helpers, 2 x 4 
 
 enum ElemKind : int { kF16 = 0, kBF16 = 1, kE4M3 = 2 };
 
+// Prefill kernel variants: a dense batch, packed variable-length sequences, or int8 codes widened
+// to 16 bits whose scores are scaled per (128-row Q block, 128-key K block) and whose O columns
+// may be scaled per channel.
+enum PrefillVariant : int { kDense = 0, kVarlen = 1, kBlockScaled = 2 };
+
 struct PrefillParams {
   void* o;                 // [B, Sq, Hq, Dv] out dtype
   float* lse;              // [B, Hq, Sq] or null
@@ -53,6 +58,12 @@ struct PrefillParams {
   const int32_t* cu_q;
   const int32_t* cu_k;
   const int32_t* tile_prefix;
+  // int8 codes (kBlockScaled): score of (row i, key j) = scale2 * q_scale[b, h, i / 128] *
+  // k_scale[b, kvh, j / 128] * (integer dot product); O column c times v_scale[b, kvh, c] if given
+  const float* q_scale;    // [B, Hq, n_qblocks]
+  const float* k_scale;    // [B, Hkv, n_kblocks]
+  const float* v_scale;    // [B, Hkv, DV] or null
+  int n_qblocks;
 };
 
 struct VarlenPrepParams {
@@ -127,6 +138,20 @@ struct MaskConvertParams {
   uint8_t* flags;
 };
 
+// int8 tensors [B, S, H, Dh] (element strides, 16-byte aligned rows) widened to contiguous
+// 16-bit copies of the same codes (every int8 value is exact in f16 and bf16).
+struct WidenSeg {
+  const int8_t* src;
+  int64_t sb, ss, sh;
+  int B, S, H, Dh;         // Dh a multiple of 16
+  void* dst;               // [B, S, H, Dh] contiguous
+};
+struct WidenParams {
+  WidenSeg seg[3];
+  int n_seg;
+  int to_bf16;             // 1: bf16 copies, 0: f16
+};
+
 // Kernel launchers (return cudaError_t of the launch).  The prefill launchers set
 // *supported = false (and launch nothing) for head dims they were not built for.
 cudaError_t launch_prefill_f16(int D, int Dv, bool causal, bool has_mask, const CUtensorMap& tq,
@@ -135,6 +160,12 @@ cudaError_t launch_prefill_f16(int D, int Dv, bool causal, bool has_mask, const 
 cudaError_t launch_prefill_bf16(int D, int Dv, bool causal, bool has_mask, const CUtensorMap& tq,
                                 const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st,
                                 bool* supported);
+cudaError_t launch_prefill_f16_block_scaled(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                                           const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st,
+                                           bool* supported);
+cudaError_t launch_prefill_bf16_block_scaled(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                                            const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st,
+                                            bool* supported);
 cudaError_t launch_prefill_e4m3(int D, int Dv, bool causal, bool has_mask, const CUtensorMap& tq,
                                 const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st,
                                 bool* supported);
@@ -150,5 +181,6 @@ bool encode_bshd(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int
                  int64_t sb, int64_t ss, int64_t sh, int box0, int box_rows, CUtensorMapSwizzle sw);
 cudaError_t launch_mask_convert(const MaskConvertParams& p, cudaStream_t st);
 cudaError_t launch_varlen_prep(const VarlenPrepParams& p, cudaStream_t st);
+cudaError_t launch_widen(const WidenParams& p, cudaStream_t st);
 
 }  // namespace sdpa

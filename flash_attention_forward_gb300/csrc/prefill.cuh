@@ -264,11 +264,13 @@ __device__ __forceinline__ int nth_item(int k) {
 // A rescale of O_t needs no barrier of its own: the commit behind s_full[t] for block j also
 // covers the P_t V of block j-1, which the same thread issued earlier.
 //   o_empty[t]              : the epilogue has read O_t (the next work tile may overwrite it)
-template <int ELEM, int D, int DV, bool CAUSAL, bool MASK, bool VARLEN>
+template <int ELEM, int D, int DV, bool CAUSAL, bool MASK, int VAR>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
   using C = PrefillCfg<ELEM, D, DV>;
+  constexpr bool VARLEN = VAR == kVarlen;
+  constexpr bool SCALED = VAR == kBlockScaled;
   constexpr int ST = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -569,6 +571,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       if (n == 0) continue;
       const int qrow = w.q0 + t * kBlockQ + row;
       const bool row_valid = qrow < w.sq;
+      // int8 codes: this tile's Q block scale folded into the exp2 scale; K block scales per block
+      float tile_scale2 = scale2;
+      const float* ks_row = nullptr;
+      if constexpr (SCALED) {
+        tile_scale2 = scale2 * __ldg(p.q_scale + (static_cast<int64_t>(w.b) * p.Hq + w.h) * p.n_qblocks +
+                                     (w.q0 + t * kBlockQ) / kBlockQ);
+        ks_row = p.k_scale + (static_cast<int64_t>(w.b) * p.Hkv + w.kvh) * p.n_kblocks + w.jb0;
+      }
       float m_used = -INFINITY;
       float l = 0.f;
       const uint4* bits_row = nullptr;
@@ -580,6 +590,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       }
 
       for (int j = 0; j < n; ++j, ++sn) {
+        float blk_scale2 = tile_scale2;  // exp2 units per unit of s in this block
+        if constexpr (SCALED) blk_scale2 = tile_scale2 * __ldg(ks_row + j);
         uint4 mbits = make_uint4(0u, 0u, 0u, 0u);
         uint32_t mflag = 0;
         if constexpr (MASK) {
@@ -641,7 +653,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           for (int c = 0; c < kBlockK; ++c)
             if ((mw[c >> 5] >> (c & 31)) & 1u) s[c] = -INFINITY;
         }
-        // block row max (scale2 > 0, so the max of s orders like the max of scale2 * s)
+        // block row max (blk_scale2 > 0, so the max of s orders like the max of blk_scale2 * s)
         float mx[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx[i] = fmaxf(s[i], s[8 + i]);
@@ -650,7 +662,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 #pragma unroll
           for (int i = 0; i < 8; ++i) mx[i] = fmax3(mx[i], s[16 * gi + i], s[16 * gi + 8 + i]);
         const float mb = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-        const float m_cand = fmaxf(m_used, mb * scale2);
+        const float m_cand = fmaxf(m_used, mb * blk_scale2);
         const bool need = m_cand > m_used + kRescaleLog2;
         const bool rescale = __any_sync(0xffffffffu, need);
         float alpha = 1.f;
@@ -659,7 +671,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           l *= alpha;
           m_used = m_cand;
         }
-        // P = exp2(scale2 * s - m), rounded to 16 bits; l sums the rounded values
+        // P = exp2(blk_scale2 * s - m), rounded to 16 bits; l sums the rounded values
         const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
         {
@@ -670,7 +682,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             for (int w2 = 0; w2 < 32; ++w2) {
               const int c = half * 64 + 2 * w2;
               float x0, x1;
-              ffma2_scalar(x0, x1, s[c], s[c + 1], scale2, neg_m);
+              ffma2_scalar(x0, x1, s[c], s[c + 1], blk_scale2, neg_m);
               pk[w2] = pack_p<ELEM>(ex2(x0), ex2(x1));
               if (w2 & 1)
                 acc_p_pair<ELEM>(ls[2], ls[3], pk[w2]);
@@ -739,12 +751,27 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         continue;
       }
       const float inv = (l > 0.f) ? p.out_scale / l : 0.f;
+      const float* vs_row = nullptr;  // int8 V codes: per-channel scales
+      if constexpr (SCALED)
+        if (p.v_scale != nullptr) vs_row = p.v_scale + (static_cast<int64_t>(w.b) * p.Hkv + w.kvh) * DV;
 #pragma unroll 1
       for (int c = 0; c < DV / 32; ++c) {
         uint32_t o[32];
         tmem_ld32(tO + c * 32, o);
         tmem_ld_wait();
         reg_fence(o);
+        if constexpr (SCALED) {
+          if (vs_row != nullptr) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 f = __ldg(reinterpret_cast<const float4*>(vs_row + c * 32) + i);
+              o[4 * i] = __float_as_uint(__uint_as_float(o[4 * i]) * f.x);
+              o[4 * i + 1] = __float_as_uint(__uint_as_float(o[4 * i + 1]) * f.y);
+              o[4 * i + 2] = __float_as_uint(__uint_as_float(o[4 * i + 2]) * f.z);
+              o[4 * i + 3] = __float_as_uint(__uint_as_float(o[4 * i + 3]) * f.w);
+            }
+          }
+        }
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
@@ -814,6 +841,13 @@ __global__ void __launch_bounds__(128) split_combine_kernel(const PrefillParams 
       acc[0] += wq * a.x, acc[1] += wq * a.y, acc[2] += wq * a.z, acc[3] += wq * a.w;
       acc[4] += wq * b.x, acc[5] += wq * b.y, acc[6] += wq * b.z, acc[7] += wq * b.w;
     }
+  }
+  if (p.v_scale != nullptr) {  // int8 V codes: per-channel scales (set only for int8 inputs)
+    const float4* vs = reinterpret_cast<const float4*>(p.v_scale + (static_cast<int64_t>(w.b) * p.Hkv + w.kvh) * DV) +
+                       2 * chunk;
+    const float4 a = __ldg(vs), b = __ldg(vs + 1);
+    acc[0] *= a.x, acc[1] *= a.y, acc[2] *= a.z, acc[3] *= a.w;
+    acc[4] *= b.x, acc[5] *= b.y, acc[6] *= b.z, acc[7] *= b.w;
   }
   const float inv = (L > 0.f) ? p.out_scale / L : 0.f;
   uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) + 2 * o_offset<false>(p, w, qrow);

@@ -5,11 +5,11 @@
 
 namespace sdpa {
 
-template <int ELEM, int D, int DV, bool CAUSAL, bool MASK, bool VARLEN>
+template <int ELEM, int D, int DV, bool CAUSAL, bool MASK, int VAR>
 cudaError_t launch_prefill_instance(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                     const PrefillParams& p, cudaStream_t st) {
   using C = PrefillCfg<ELEM, D, DV>;
-  auto kern = prefill_kernel<ELEM, D, DV, CAUSAL, MASK, VARLEN>;
+  auto kern = prefill_kernel<ELEM, D, DV, CAUSAL, MASK, VAR>;
   // the shared-memory opt-in is per device; setting it again is harmless
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
@@ -33,7 +33,7 @@ cudaError_t launch_prefill_instance(const CUtensorMap& tq, const CUtensorMap& tk
   const long long kv_units = (long long)p.B * p.Hkv;
   q.units_per_group = (int)(ug < 1 ? 1 : (ug > kv_units ? kv_units : ug));
   kern<<<grid, kPrefillThreads, C::SMEM, st>>>(tq, tk, tv, q);
-  if (!CAUSAL && !VARLEN && p.split_parts > 1) {
+  if (!CAUSAL && VAR != kVarlen && p.split_parts > 1) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const long long threads = (long long)p.split_tail * kCtaRows * (DV / 8);
     split_combine_kernel<ELEM == kE4M3 ? kBF16 : ELEM, DV><<<(unsigned)((threads + 127) / 128), 128, 0, st>>>(q);
@@ -45,13 +45,21 @@ template <int ELEM, int D, int DV>
 cudaError_t launch_prefill_dims(bool causal, bool has_mask, const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st) {
   if (p.varlen)  // packed sequences: no mask, no split tail
-    return causal ? launch_prefill_instance<ELEM, D, DV, true, false, true>(tq, tk, tv, p, st)
-                  : launch_prefill_instance<ELEM, D, DV, false, false, true>(tq, tk, tv, p, st);
+    return causal ? launch_prefill_instance<ELEM, D, DV, true, false, kVarlen>(tq, tk, tv, p, st)
+                  : launch_prefill_instance<ELEM, D, DV, false, false, kVarlen>(tq, tk, tv, p, st);
   if (causal)
-    return has_mask ? launch_prefill_instance<ELEM, D, DV, true, true, false>(tq, tk, tv, p, st)
-                    : launch_prefill_instance<ELEM, D, DV, true, false, false>(tq, tk, tv, p, st);
-  return has_mask ? launch_prefill_instance<ELEM, D, DV, false, true, false>(tq, tk, tv, p, st)
-                  : launch_prefill_instance<ELEM, D, DV, false, false, false>(tq, tk, tv, p, st);
+    return has_mask ? launch_prefill_instance<ELEM, D, DV, true, true, kDense>(tq, tk, tv, p, st)
+                    : launch_prefill_instance<ELEM, D, DV, true, false, kDense>(tq, tk, tv, p, st);
+  return has_mask ? launch_prefill_instance<ELEM, D, DV, false, true, kDense>(tq, tk, tv, p, st)
+                  : launch_prefill_instance<ELEM, D, DV, false, false, kDense>(tq, tk, tv, p, st);
+}
+
+// int8 codes widened to 16 bits (Q/K/V already in the 16-bit type), per-block score scales.
+template <int ELEM, int D>
+cudaError_t launch_prefill_block_scaled(bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                                        const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st) {
+  return causal ? launch_prefill_instance<ELEM, D, D, true, false, kBlockScaled>(tq, tk, tv, p, st)
+                : launch_prefill_instance<ELEM, D, D, false, false, kBlockScaled>(tq, tk, tv, p, st);
 }
 
 }  // namespace sdpa

@@ -49,7 +49,7 @@ typedef enum {
   SDPA_ERR_TIMEOUT = 4      /* a kernel's bounded wait gave up (see sdpa_check_device_status) */
 } sdpa_status;
 
-typedef enum { SDPA_F16 = 0, SDPA_BF16 = 1, SDPA_E4M3 = 2 } sdpa_dtype;
+typedef enum { SDPA_F16 = 0, SDPA_BF16 = 1, SDPA_E4M3 = 2, SDPA_I8 = 3 } sdpa_dtype;
 
 /* Number of int64 entries in the prefill stride array. */
 #define SDPA_FWD_NSTRIDES 12
@@ -171,6 +171,47 @@ int sdpa_fwd_varlen_fp8(const void* q, const void* k, const void* v, void* o, fl
                         int total_k, int max_seqlen_q, int D, int Dv, const int64_t* strides, float scale, int causal,
                         void* workspace, size_t workspace_bytes, float descale_q, float descale_k, float descale_v,
                         sdpa_dtype out_dtype, void* stream);
+
+/*
+ * sdpa_fwd_int8_workspace_size -- bytes of device scratch sdpa_fwd_int8 needs: the 16-bit copies
+ * of the int8 operands (Q and K, plus V when v_int8 != 0; B*S*H*D*2 bytes each, rounded up to 16)
+ * followed by the optional split partials described under sdpa_fwd_workspace_size.  Sizes below
+ * 1 give 0.
+ */
+size_t sdpa_fwd_int8_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, int v_int8, int causal);
+
+/*
+ * sdpa_fwd_int8 -- prefill with int8 Q/K codes and per-block scales (page "Xe SDPA Forward
+ * Mainloop", section "SageV1 concrete instance": the SageV1 prefill takes its Q/K dtype, a P.V
+ * dtype, scale pointers and a use_int8_pv switch, and has launchers for head dims 64 and 128).
+ * With Q = q_code * q_scale[b, h, i / 128] and K = k_code * k_scale[b, kvh, j / 128]:
+ *
+ *     s[j] = scale * q_scale[b,h,i/128] * k_scale[b,kvh,j/128] * dot(q_code[b,i,h,:], k_code[b,j,kvh,:])
+ *
+ * then softmax, O and LSE as in sdpa_fwd.  V is either 16-bit values (v_dtype == out_dtype) or
+ * int8 codes (v_dtype == SDPA_I8) with per-channel scales: V[b,j,kvh,c] = v_code * v_scale[b,kvh,c].
+ * sm_103a has no int8 tensor-core MMA, so a first kernel copies the codes into 16-bit form (exact)
+ * in the workspace and the prefill multiplies them on the 16-bit tensor cores; the integer dot
+ * products are exact in the fp32 accumulator (|sum| < 2^24), so the scores equal an int32
+ * accumulation times the scales.  P is rounded to out_dtype; the v_scale factor multiplies the
+ * accumulated O columns.
+ *
+ *   q [B, Sq, Hq, D] int8    k [B, Sk, Hkv, D] int8    v [B, Sk, Hkv, D] int8 or out_dtype
+ *   o [B, Sq, Hq, D] out_dtype; lse [B, Hq, Sq] fp32 or NULL
+ *   strides: NULL or the 12 element strides of sdpa_fwd; int8 strides multiples of 16 elements,
+ *            16-bit strides multiples of 8; q, k (and int8 v) 16-byte aligned
+ *   q_scale  DEVICE fp32 [B, Hq, ceil(Sq / 128)], contiguous; k_scale DEVICE fp32 [B, Hkv,
+ *            ceil(Sk / 128)], contiguous; both 4-byte aligned; positive finite values expected
+ *   v_scale  DEVICE fp32 [B, Hkv, D], contiguous, 16-byte aligned, when v_dtype == SDPA_I8; else NULL
+ *   workspace: at least the copy part of sdpa_fwd_int8_workspace_size(...), 16-byte aligned
+ *   D = Dv in {64, 128}; out_dtype SDPA_F16 or SDPA_BF16 (the copies and P use that type); no
+ *   additive mask.  Other arguments as in sdpa_fwd.  Two kernels run in `stream` (the copy, then
+ *   the prefill; plus the split merge when it applies).
+ */
+int sdpa_fwd_int8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,
+                  int Sk, int D, const int64_t* strides, const float* q_scale, const float* k_scale,
+                  const float* v_scale, float scale, int causal, void* workspace, size_t workspace_bytes,
+                  sdpa_dtype v_dtype, sdpa_dtype out_dtype, void* stream);
 
 /*
  * sdpa_decode_workspace_size -- bytes of device scratch sdpa_decode needs for per-split

@@ -105,6 +105,30 @@ def sdpa_fwd(q, k, v, mask=None, *, scale: float, causal: bool = False, rows=Non
     return o, lse
 
 
+def dequantize_int8(codes, scales, block: int | None):
+    """fp64 values of int8 codes [B, S, H, D]: code * scale with scales [B, H, ceil(S / block)]
+    (one per block of rows) or, for block=None, [B, H, D] (one per channel)."""
+    c = as_f64(codes)
+    sc = as_f64(scales)
+    if block is None:
+        return c * sc[:, None, :, :]
+    rows = np.arange(c.shape[1]) // block  # block of each row
+    return c * sc[:, :, rows].transpose(0, 2, 1)[..., None]
+
+
+def sdpa_fwd_int8(q, k, v, q_scale, k_scale, v_scale=None, *, scale: float, causal: bool = False, rows=None,
+                  block: int = 128, nthreads: int | None = None):
+    """O and LSE of attention over int8 codes in fp64: Q = q_code * q_scale[b, h, i / block],
+    K = k_code * k_scale[b, kvh, j / block], V = v values or v_code * v_scale[b, kvh, c] (page "Xe SDPA
+    Forward Mainloop", section "SageV1 concrete instance": Q/K dtype, P.V dtype and scale pointers).
+    The dequantised operands go through sdpa_fwd, so s = scale * q_scale * k_scale * (integer dot
+    product), exactly up to fp64 rounding."""
+    qd = dequantize_int8(q, q_scale, block)
+    kd = dequantize_int8(k, k_scale, block)
+    vd = as_f64(v) if v_scale is None else dequantize_int8(v, v_scale, None)
+    return sdpa_fwd(qd, kd, vd, scale=scale, causal=causal, rows=rows, nthreads=nthreads)
+
+
 def _offsets(cu):
     return [int(x) for x in (cu.tolist() if hasattr(cu, "tolist") else cu)]
 

@@ -358,3 +358,62 @@ def test_varlen_rows_and_unowned_rows():
         assert np.array_equal(os_[n], o[i, h]) and ls[n] == lse[h, i]
     with pytest.raises(AssertionError):
         oracle.sdpa_fwd_varlen(x["q"], x["k"], x["v"], x["cu_q"], x["cu_k"], scale=0.3, rows=[[10, 0]])
+
+
+def _torch_dequant_blocks(codes, scales, block):
+    """Independent dequantisation with torch ops: each row's scale repeated over its block."""
+    S = codes.shape[1]
+    per_row = scales.double().repeat_interleave(block, dim=2)[:, :, :S]  # [B, H, S]
+    return codes.double() * per_row.permute(0, 2, 1).unsqueeze(-1)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("v_int8", [False, True])
+def test_int8_oracle_matches_torch_on_dequantized_operands(causal, v_int8):
+    g = torch.Generator().manual_seed(51)
+    B, Sq, Sk, Hq, Hkv, D = 2, 300, 260, 4, 2, 16
+    q = torch.randint(-127, 128, (B, Sq, Hq, D), generator=g, dtype=torch.int8)
+    k = torch.randint(-127, 128, (B, Sk, Hkv, D), generator=g, dtype=torch.int8)
+    qs = torch.rand((B, Hq, 3), generator=g) * 0.02 + 0.001
+    ks = torch.rand((B, Hkv, 3), generator=g) * 0.02 + 0.001
+    if v_int8:
+        v = torch.randint(-127, 128, (B, Sk, Hkv, D), generator=g, dtype=torch.int8)
+        vs = torch.rand((B, Hkv, D), generator=g) * 0.01 + 0.001
+        vt = v.double() * vs.double().unsqueeze(1)
+    else:
+        v, vs = _rand((B, Sk, Hkv, D), 52).to(torch.float16), None
+        vt = v.double()
+    o, lse = oracle.sdpa_fwd_int8(q, k, v, qs, ks, vs, scale=0.25, causal=causal)
+    qt, kt = _torch_dequant_blocks(q, qs, 128), _torch_dequant_blocks(k, ks, 128)
+    ref = _torch_sdpa(qt, kt, vt, None, 0.25, causal).numpy()
+    ref_lse = _torch_lse(qt, kt, None, 0.25, causal).numpy()
+    assert np.abs(o - ref).max() <= 1e-12
+    assert np.abs(lse - ref_lse).max() <= 1e-12
+
+
+def test_int8_block_scale_acts_on_its_rows_only():
+    # doubling the scale of Q block 1 (rows 128..255) of one head changes exactly those rows
+    x = workloads.int8_prefill(1, 2, 1, 300, 200, 32, seed=53)
+    o1, l1 = oracle.sdpa_fwd_int8(x["q"], x["k"], x["v"], x["q_scale"], x["k_scale"], scale=0.2)
+    qs = x["q_scale"].clone()
+    qs[0, 1, 1] *= 2.0
+    o2, l2 = oracle.sdpa_fwd_int8(x["q"], x["k"], x["v"], qs, x["k_scale"], scale=0.2)
+    changed = np.abs(l2 - l1)[0] > 0  # [Hq, Sq]
+    assert not changed[0].any()
+    assert changed[1, 128:256].all() and not changed[1, :128].any() and not changed[1, 256:].any()
+    assert np.array_equal(o1[0, :128], o2[0, :128]) and np.array_equal(o1[0, 256:], o2[0, 256:])
+
+
+def test_int8_quantization_recipe():
+    x = torch.randn(2, 300, 3, 16, generator=torch.Generator().manual_seed(54))
+    x[1, 128:256, 2] = 0.0  # an all-zero block gets scale 1 and zero codes
+    codes, scales = workloads.quantize_int8_blocks(x)
+    assert scales.shape == (2, 3, 3) and codes.dtype == torch.int8
+    deq = _torch_dequant_blocks(codes, scales, 128)
+    per_row = scales.repeat_interleave(128, dim=2)[:, :, :300].permute(0, 2, 1).unsqueeze(-1)
+    assert bool(((deq - x.double()).abs() <= per_row.double() / 2 + 1e-12).all())
+    assert scales[1, 2, 1] == 1.0 and int(codes[1, 128:256, 2].abs().max()) == 0
+    assert int(codes.abs().max()) == 127
+    vc, vs = workloads.quantize_int8_channels(x)
+    assert vs.shape == (2, 3, 16)
+    assert bool(((vc.double() * vs.double().unsqueeze(1) - x.double()).abs() <= vs.double().unsqueeze(1) / 2 + 1e-12).all())

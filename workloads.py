@@ -72,6 +72,9 @@ WORKLOADS = {
                  dtype="bf16", dist="normal", out_dtype="bf16", kv_len_range=(1024, 16384)),
         Workload("mla_fp8_causal_prefill_d192", 5, "prefill", B=1, Hq=128, Hkv=128, Sq=8192, Sk=8192, D=192,
                  Dv=128, dtype="e4m3", dist="normal", causal=True, out_dtype="bf16"),
+        # int8 Q/K codes with per-128-row-block scales, fp16 V (the SageV1 instance's head dim 128)
+        Workload("int8_qk_causal_prefill_d128", 7, "prefill", B=2, Hq=32, Hkv=8, Sq=4096, Sk=4096, D=128,
+                 Dv=128, dtype="i8", dist="normal", causal=True, out_dtype="f16", extra={"v": "f16"}),
         # packed sequences: B sequence lengths drawn uniformly from len_range, keys = queries
         Workload("varlen_causal_prefill_bf16_d128", 6, "varlen", B=16, Hq=32, Hkv=8, Sq=8192, Sk=8192, D=128,
                  Dv=128, dtype="bf16", dist="normal", causal=True, out_dtype="bf16",
@@ -81,7 +84,9 @@ WORKLOADS = {
 
 BY_INDEX = {w.index: w for w in WORKLOADS.values()}
 
-_TORCH_DTYPE = {"f16": torch.float16, "bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn}
+_TORCH_DTYPE = {"f16": torch.float16, "bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn, "i8": torch.int8}
+INT8_MAX = 127.0
+INT8_BLOCK = 128  # rows per Q / K scale block
 
 
 def torch_dtype(name: str) -> torch.dtype:
@@ -108,6 +113,53 @@ def quantize_e4m3(x: torch.Tensor):
     s = amax / E4M3_MAX if amax > 0 else 1.0
     codes = (x / s).to(torch.float8_e4m3fn)
     return codes, s
+
+
+def quantize_int8_blocks(x: torch.Tensor, block: int = INT8_BLOCK):
+    """Symmetric int8 codes of an fp32 [B, S, H, D] tensor with one scale per (b, h, block of
+    ``block`` rows): scale = amax / 127 over the block's rows and channels (1 for an all-zero
+    block), code = round-half-even(x / scale), which stays within [-127, 127].  Returns (codes
+    [B, S, H, D] int8, scales [B, H, ceil(S / block)] fp32)."""
+    B, S, H, D = x.shape
+    nb = (S + block - 1) // block
+    pad = torch.zeros((B, nb * block, H, D), dtype=torch.float32)
+    pad[:, :S] = x
+    amax = pad.view(B, nb, block, H, D).abs().amax(dim=(2, 4)).transpose(1, 2)  # [B, H, nb]
+    scales = torch.where(amax > 0, amax / INT8_MAX, torch.ones_like(amax)).to(torch.float32).contiguous()
+    per_row = scales.transpose(1, 2).repeat_interleave(block, dim=1)[:, :S]  # [B, S, H]
+    codes = torch.round(x / per_row.unsqueeze(-1)).clamp(-INT8_MAX, INT8_MAX).to(torch.int8)
+    return codes, scales
+
+
+def quantize_int8_channels(x: torch.Tensor):
+    """Symmetric int8 codes of an fp32 [B, S, H, D] tensor with one scale per (b, h, channel):
+    amax over the rows / 127.  Returns (codes int8, scales [B, H, D] fp32)."""
+    amax = x.abs().amax(dim=1)  # [B, H, D]
+    scales = torch.where(amax > 0, amax / INT8_MAX, torch.ones_like(amax)).to(torch.float32).contiguous()
+    codes = torch.round(x / scales.unsqueeze(1)).clamp(-INT8_MAX, INT8_MAX).to(torch.int8)
+    return codes, scales
+
+
+def int8_prefill(B, Hq, Hkv, Sq, Sk, D, v="f16", dist="normal", seed=0):
+    """int8 Q/K codes with per-block scales; V as fp16 / bf16 values, or (v="i8") int8 codes with
+    per-channel scales.  Draw order q, k, v in fp32, then quantisation."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    qf = _draw(g, (B, Sq, Hq, D), dist)
+    kf = _draw(g, (B, Sk, Hkv, D), dist)
+    vf = _draw(g, (B, Sk, Hkv, D), dist)
+    q, q_scale = quantize_int8_blocks(qf)
+    k, k_scale = quantize_int8_blocks(kf)
+    if v == "i8":
+        vv, v_scale = quantize_int8_channels(vf)
+    else:
+        vv, v_scale = vf.to(_TORCH_DTYPE[v]), None
+    return {"q": q, "k": k, "v": vv, "q_scale": q_scale, "k_scale": k_scale, "v_scale": v_scale}
+
+
+def int8_inputs(w: Workload, rotation: int = 0):
+    return int8_prefill(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, v=w.extra.get("v", "f16"), dist=w.dist,
+                        seed=1000 * w.index + rotation)
 
 
 def _store(x: torch.Tensor, dtype: str):
