@@ -13,10 +13,12 @@ Entry points (same names as the C ABI):
     sdpa_fwd_varlen(q, k, v, cu_q, cu_k, max_seqlen_q, ...)   prefill of packed sequences
     sdpa_fwd_varlen_fp8(q, k, v, cu_q, cu_k, max_seqlen_q, dq, dk, dv, ...)   the same in e4m3
     sdpa_fwd_int8(q, k, v, q_scale, k_scale, v_scale, ...)   int8 Q/K codes with per-block scales
+    sdpa_fwd_host(q, k, v, ...)                 sdpa_fwd on pinned host tensors, copies overlapped
     sdpa_decode(q, k_cache, v_cache, kv_len, ...)   two-phase split-KV decode
     sdpa_decode_paged(q, k_pool, v_pool, page_table, kv_len, ...)   the same over a paged cache
     sdpa_decode_noalloc(q, k_cache, v_cache, kv_len, ...)   the same with library-owned scratch
     sdpa_fwd_workspace_size, sdpa_fwd_varlen_workspace_size, sdpa_fwd_int8_workspace_size,
+    sdpa_fwd_host_workspace_size,
     sdpa_decode_workspace_size,
     sdpa_check_device_status,
     sdpa_status_string, sdpa_version
@@ -76,6 +78,10 @@ def _load():
         lib.sdpa_fwd_int8_workspace_size.restype = sz
         lib.sdpa_fwd_int8.argtypes = [p, p, p, p, p, i, i, i, i, i, i, p, p, p, p, f, i, p, sz, i, i, p]
         lib.sdpa_fwd_int8.restype = i
+        lib.sdpa_fwd_host_workspace_size.argtypes = [i, i, i, i, i, i, i, i]
+        lib.sdpa_fwd_host_workspace_size.restype = sz
+        lib.sdpa_fwd_host.argtypes = [p, p, p, p, p, i, i, i, i, i, i, i, f, i, p, sz, i, i, p]
+        lib.sdpa_fwd_host.restype = i
         lib.sdpa_decode_workspace_size.argtypes = [i, i, i, i]
         lib.sdpa_decode_workspace_size.restype = sz
         lib.sdpa_decode.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, p, f, p, sz, i, p]
@@ -316,6 +322,44 @@ def sdpa_fwd_int8(q, k, v, q_scale, k_scale, v_scale=None, *, scale: float | Non
                                _ptr(workspace), workspace.numel() * workspace.element_size(), _DT[v.dtype],
                                _DT[out.dtype], _stream_ptr(stream))
     _check("sdpa_fwd_int8", rc)
+    return out, lse
+
+
+def sdpa_fwd_host_workspace_size(B: int, Hq: int, Hkv: int, Sq: int, Sk: int, D: int, Dv: int,
+                                 causal: bool) -> int:
+    """Bytes of device workspace for sdpa_fwd_host (device copies of Q, K, V, O, LSE + split partials)."""
+    return int(_load().sdpa_fwd_host_workspace_size(B, Hq, Hkv, Sq, Sk, D, Dv, int(bool(causal))))
+
+
+def sdpa_fwd_host(q, k, v, *, scale: float | None = None, causal: bool = False, out=None, lse=None,
+                  return_lse: bool = True, workspace=None, device=None, stream=None):
+    """sdpa_fwd on CPU tensors (pinned for overlap): copies up, computes and copies back in chunks of
+    query rows, overlapping the three.  q [B,Sq,Hq,D], k [B,Sk,Hkv,D], v [B,Sk,Hkv,Dv] contiguous
+    fp16/bf16 CPU tensors.  Returns (o, lse) CPU tensors, valid once the stream is synchronized."""
+    for t in (q, k, v):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("sdpa_fwd_host takes contiguous CPU tensors")
+    if q.dtype not in (torch.float16, torch.bfloat16) or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("sdpa_fwd_host takes fp16 or bf16 inputs of one type")
+    B, Sq, Hq, D = q.shape
+    _, Sk, Hkv, _ = k.shape
+    Dv = v.shape[-1]
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty((B, Sq, Hq, Dv), dtype=q.dtype).pin_memory()
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32).pin_memory()
+    for t, shape in ((out, (B, Sq, Hq, Dv)), (lse, (B, Hq, Sq))):
+        if t is not None and (t.is_cuda or not t.is_contiguous() or tuple(t.shape) != shape):
+            raise ValueError(f"outputs must be contiguous CPU tensors of shape {shape}")
+    if workspace is None:
+        workspace = torch.empty(sdpa_fwd_host_workspace_size(B, Hq, Hkv, Sq, Sk, D, Dv, causal), dtype=torch.uint8,
+                                device=dev)
+    rc = _load().sdpa_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk, D, Dv, scale,
+                               int(bool(causal)), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                               _DT[q.dtype], _DT[out.dtype], _stream_ptr(stream))
+    _check("sdpa_fwd_host", rc)
     return out, lse
 
 

@@ -1,6 +1,7 @@
 // C ABI of the library (declared in include/sdpa.h): argument validation, tensor-map
 // encoding, instance dispatch and the device status word.  No entry point allocates
 // device memory; every argument is checked before the first CUDA call.
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <atomic>
@@ -132,7 +133,8 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
                int Sk, int D, int Dv, const int64_t* strides, float scale, int causal, const void* mask,
                const int64_t* mask_strides, void* workspace, size_t workspace_bytes, int elem, float descale_q,
                float descale_k, float descale_v, sdpa_dtype out_dtype, void* stream,
-               const VarlenArgs* vl = nullptr, const Int8Args* i8 = nullptr) {
+               const VarlenArgs* vl = nullptr, const Int8Args* i8 = nullptr, int causal_off = 0,
+               int64_t lse_ld = 0) {
   // ---- validation (no CUDA call before this block passes)
   if (!q || !k || !v || !o) return SDPA_ERR_INVALID;
   if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Sk < 1 || D < 1 || Dv < 1) return SDPA_ERR_INVALID;
@@ -230,6 +232,8 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   p.lse = lse;
   p.o_b = st[9], p.o_s = st[10], p.o_h = st[11];
   p.B = B, p.Hq = Hq, p.Hkv = Hkv, p.Sq = Sq, p.Sk = Sk;
+  p.lse_ld = lse_ld > 0 ? lse_ld : Sq;
+  p.causal_off = causal_off;
   p.group = Hq / Hkv;
   p.n_cta_tiles = n_cta_tiles;
   p.n_kblocks = n_kblocks;
@@ -431,6 +435,134 @@ int sdpa_fwd_int8(const void* q, const void* k, const void* v, void* o, float* l
   return fwd_common(q16, k16, v16, o, lse, B, Hq, Hkv, Sq, Sk, D, D, st16, scale, causal, nullptr, nullptr,
                     ws + wide, workspace_bytes - wide, out_dtype == SDPA_BF16 ? kBF16 : kF16, 1.f, 1.f, 1.f,
                     out_dtype, stream, nullptr, &a);
+}
+
+namespace {
+constexpr int kMaxHostChunks = 8;
+
+// Per device: the two copy streams and the events of sdpa_fwd_host, created on first use and
+// kept for the life of the process.
+struct HostPipe {
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t ev[2 * kMaxHostChunks + 2] = {};
+};
+HostPipe g_pipe[kMaxDevices];
+std::mutex g_pipe_mu;  // held while a call enqueues (the events are shared)
+
+cudaError_t host_pipe(int dev, HostPipe** out) {
+  HostPipe& hp = g_pipe[dev];
+  cudaError_t e;
+  if (hp.h2d == nullptr) {
+    if ((e = cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    for (cudaEvent_t& ev : hp.ev)
+      if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess) return e;
+  }
+  *out = &hp;
+  return cudaSuccess;
+}
+
+struct HostLayout {
+  size_t q, k, v, o, lse, total;  // byte offsets of the device copies in the workspace, and their end
+};
+
+HostLayout host_layout(int B, int Hq, int Hkv, int Sq, int Sk, int D, int Dv, size_t esize) {
+  HostLayout L{};
+  L.q = 0;
+  L.k = L.q + round16((size_t)B * Sq * Hq * D * esize);
+  L.v = L.k + round16((size_t)B * Sk * Hkv * D * esize);
+  L.o = L.v + round16((size_t)B * Sk * Hkv * Dv * esize);
+  L.lse = L.o + round16((size_t)B * Sq * Hq * Dv * 2);
+  L.total = L.lse + round16((size_t)B * Hq * Sq * 4);
+  return L;
+}
+
+// Query rows per chunk: whole 256-row work tiles, at most kMaxHostChunks chunks.
+int host_chunk_rows(int Sq) {
+  const int per = (Sq + kMaxHostChunks - 1) / kMaxHostChunks;
+  return std::max(kCtaRows, (per + kCtaRows - 1) / kCtaRows * kCtaRows);
+}
+}  // namespace
+
+size_t sdpa_fwd_host_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, int Dv, int causal) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Sk < 1 || D < 1 || Dv < 1) return 0;
+  const int rows = host_chunk_rows(Sq);
+  return host_layout(B, Hq, Hkv, Sq, Sk, D, Dv, 2).total +
+         prefill_split_bytes(fwd_split_plan(B, Hq, std::min(rows, Sq), Sk, causal != 0), Dv);
+}
+
+int sdpa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,
+                  int Sk, int D, int Dv, float scale, int causal, void* workspace, size_t workspace_bytes,
+                  sdpa_dtype in_dtype, sdpa_dtype out_dtype, void* stream) {
+  // ---- validation (no CUDA call before this block passes)
+  if (!q || !k || !v || !o) return SDPA_ERR_INVALID;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Sk < 1 || D < 1 || Dv < 1 || Hq % Hkv != 0) return SDPA_ERR_INVALID;
+  if (!(std::isfinite(scale) && scale > 0.f)) return SDPA_ERR_INVALID;
+  if (in_dtype != SDPA_F16 && in_dtype != SDPA_BF16) return SDPA_ERR_UNSUPPORTED;
+  if (out_dtype != in_dtype) return SDPA_ERR_UNSUPPORTED;
+  if (!((D == 64 && Dv == 64) || (D == 128 && Dv == 128) || (D == 192 && Dv == 128))) return SDPA_ERR_UNSUPPORTED;
+  const HostLayout L = host_layout(B, Hq, Hkv, Sq, Sk, D, Dv, 2);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < L.total) return SDPA_ERR_INVALID;
+  const int rows = host_chunk_rows(Sq);
+  const int n_chunks = (Sq + rows - 1) / rows;
+  if ((long long)((rows + kCtaRows - 1) / kCtaRows) * B * Hq * kMaxSplitParts >= (1ll << 31))
+    return SDPA_ERR_UNSUPPORTED;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SDPA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_pipe_mu);
+  HostPipe* hp = nullptr;
+  if (host_pipe(dev, &hp) != cudaSuccess) return SDPA_ERR_CUDA;
+  cudaStream_t stm = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  char *dq = ws + L.q, *dk = ws + L.k, *dv = ws + L.v, *dO = ws + L.o;
+  float* dl = reinterpret_cast<float*>(ws + L.lse);
+  const size_t qrow = (size_t)Hq * D * 2, krow = (size_t)Hkv * D * 2, vrow = (size_t)Hkv * Dv * 2,
+               orow = (size_t)Hq * Dv * 2;
+  const int64_t st[SDPA_FWD_NSTRIDES] = {(int64_t)Sq * Hq * D,   (int64_t)Hq * D,  D,
+                                         (int64_t)Sk * Hkv * D,  (int64_t)Hkv * D, D,
+                                         (int64_t)Sk * Hkv * Dv, (int64_t)Hkv * Dv, Dv,
+                                         (int64_t)Sq * Hq * Dv,  (int64_t)Hq * Dv, Dv};
+  // B rows of `bytes` starting at row r of a [B, S, ...] tensor whose rows are `row` bytes
+  auto copy_rows = [&](void* dst, const void* src, size_t row, int S, int r0, int r1, cudaMemcpyKind kind,
+                       cudaStream_t s) {
+    const size_t off = (size_t)r0 * row, pitch = (size_t)S * row;
+    return cudaMemcpy2DAsync(static_cast<char*>(dst) + off, pitch, static_cast<const char*>(src) + off, pitch,
+                             (size_t)(r1 - r0) * row, B, kind, s);
+  };
+  cudaEvent_t* ev_in = hp->ev;                    // chunk inputs on the device
+  cudaEvent_t* ev_out = hp->ev + kMaxHostChunks;  // chunk outputs computed
+  cudaEvent_t ev_start = hp->ev[2 * kMaxHostChunks], ev_done = hp->ev[2 * kMaxHostChunks + 1];
+  // the device copies may still be in use by earlier work in `stream`
+  if (cudaEventRecord(ev_start, stm) != cudaSuccess || cudaStreamWaitEvent(hp->h2d, ev_start, 0) != cudaSuccess)
+    return SDPA_ERR_CUDA;
+  // K and V go up first, whole (one copy each: every copy command costs the copy engine a few
+  // microseconds, and the total time of the upward copies, not their order, sets the pace);
+  // then Q chunk by chunk
+  if (cudaMemcpyAsync(dk, k, (size_t)B * Sk * krow, cudaMemcpyHostToDevice, hp->h2d) != cudaSuccess ||
+      cudaMemcpyAsync(dv, v, (size_t)B * Sk * vrow, cudaMemcpyHostToDevice, hp->h2d) != cudaSuccess)
+    return SDPA_ERR_CUDA;
+  for (int c = 0; c < n_chunks; ++c) {
+    const int r0 = c * rows, r1 = std::min(Sq, r0 + rows);
+    // causal (top-left): rows r0..r1-1 see keys below r1; otherwise every key
+    const int k_need = causal ? std::min(Sk, r1) : Sk;
+    if (copy_rows(dq, q, qrow, Sq, r0, r1, cudaMemcpyHostToDevice, hp->h2d) != cudaSuccess) return SDPA_ERR_CUDA;
+    if (cudaEventRecord(ev_in[c], hp->h2d) != cudaSuccess || cudaStreamWaitEvent(stm, ev_in[c], 0) != cudaSuccess)
+      return SDPA_ERR_CUDA;
+    const int rc = fwd_common(dq + (size_t)r0 * qrow, dk, dv, dO + (size_t)r0 * orow, lse ? dl + r0 : nullptr, B, Hq,
+                              Hkv, r1 - r0, std::max(k_need, 1), D, Dv, st, scale, causal, nullptr, nullptr,
+                              ws + L.total, workspace_bytes - L.total, in_dtype == SDPA_BF16 ? kBF16 : kF16, 1.f, 1.f,
+                              1.f, out_dtype, stream, nullptr, nullptr, causal ? r0 : 0, Sq);
+    if (rc != SDPA_OK) return rc;
+    if (cudaEventRecord(ev_out[c], stm) != cudaSuccess || cudaStreamWaitEvent(hp->d2h, ev_out[c], 0) != cudaSuccess)
+      return SDPA_ERR_CUDA;
+    if (copy_rows(o, dO, orow, Sq, r0, r1, cudaMemcpyDeviceToHost, hp->d2h) != cudaSuccess) return SDPA_ERR_CUDA;
+  }
+  if (lse && cudaMemcpyAsync(lse, dl, (size_t)B * Hq * Sq * 4, cudaMemcpyDeviceToHost, hp->d2h) != cudaSuccess)
+    return SDPA_ERR_CUDA;
+  if (cudaEventRecord(ev_done, hp->d2h) != cudaSuccess || cudaStreamWaitEvent(stm, ev_done, 0) != cudaSuccess)
+    return SDPA_ERR_CUDA;
+  return SDPA_OK;
 }
 
 size_t sdpa_decode_workspace_size(int B, int Hq, int max_kv, int Dv) {

@@ -32,6 +32,8 @@ struct PrefillParams {
   float* lse;              // [B, Hq, Sq] or null
   int64_t o_b, o_s, o_h;   // element strides of o
   int B, Hq, Hkv, Sq, Sk;
+  int causal_off;          // causal: key j visible to query row i iff j <= i + causal_off (top-left: 0)
+  int64_t lse_ld;          // dense LSE layout [B, Hq, lse_ld] (lse_ld >= Sq)
   int group;               // Hq / Hkv
   int n_cta_tiles;         // ceil(Sq / kCtaRows)
   int units_per_group;     // KV units (batch x KV head) whose work tiles are scheduled together

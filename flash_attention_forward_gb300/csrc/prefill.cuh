@@ -147,7 +147,7 @@ __device__ __forceinline__ int64_t lse_index(const PrefillParams& p, const WorkT
   if constexpr (VARLEN)
     return static_cast<int64_t>(w.h) * p.total_q + w.q_off + qrow;
   else
-    return (static_cast<int64_t>(w.b) * p.Hq + w.h) * p.Sq + qrow;
+    return (static_cast<int64_t>(w.b) * p.Hq + w.h) * p.lse_ld + qrow;
 }
 
 // Work tiles in launch order.  A KV unit is one (batch, KV head): its K/V are shared by the
@@ -230,7 +230,7 @@ __device__ __forceinline__ WorkTile work_tile(const PrefillParams& p, int work_u
       n = jb1 - w.jb0;
       if (CAUSAL) {
         const int last_row = min(r0 + kBlockQ - 1, w.sq - 1);
-        n = min(n, last_row / kBlockK + 1);
+        n = min(n, (last_row + p.causal_off) / kBlockK + 1);
       }
     }
     w.n_t[t] = n;
@@ -627,9 +627,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
         // the causal diagonal and the ragged last block: hide keys past the row / past Sk
         const int k0 = (w.jb0 + j) * kBlockK;
-        const bool edge = (CAUSAL && (k0 + kBlockK - 1 > w.q0 + t * kBlockQ)) || (k0 + kBlockK > w.sk);
+        const bool edge = (CAUSAL && (k0 + kBlockK - 1 > w.q0 + t * kBlockQ + p.causal_off)) || (k0 + kBlockK > w.sk);
         if (edge) {
-          const int lim = (CAUSAL ? min(w.sk, qrow + 1) : w.sk) - k0;
+          const int lim = (CAUSAL ? min(w.sk, qrow + p.causal_off + 1) : w.sk) - k0;
 #pragma unroll
           for (int c = 0; c < kBlockK; ++c)
             if (c >= lim) s[c] = -INFINITY;

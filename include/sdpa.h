@@ -173,6 +173,36 @@ int sdpa_fwd_varlen_fp8(const void* q, const void* k, const void* v, void* o, fl
                         sdpa_dtype out_dtype, void* stream);
 
 /*
+ * sdpa_fwd_host_workspace_size -- bytes of device scratch sdpa_fwd_host needs: device copies of
+ * Q, K, V, O and LSE (contiguous, each rounded up to 16 bytes), then the optional split partials
+ * of one chunk (see sdpa_fwd_workspace_size).  Sizes below 1 give 0.
+ */
+size_t sdpa_fwd_host_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, int Dv, int causal);
+
+/*
+ * sdpa_fwd_host -- sdpa_fwd on HOST buffers: copies the inputs to the device, computes, and
+ * copies O (and LSE) back, overlapping the three.  K and V go up first on a copy stream, then
+ * Q in at most 8 chunks of whole 256-row work tiles; chunk c's prefill runs in `stream` as soon
+ * as its rows have landed (over the keys those rows see, causal masking counted from the
+ * chunk's global row), and its O rows come back on a second copy stream while later chunks are
+ * still copying or computing.  Results equal sdpa_fwd's on the same inputs (causal: bit for bit).
+ *
+ *   q, k, v, o, lse: HOST pointers, contiguous [B, Sq, Hq, D], [B, Sk, Hkv, D], [B, Sk, Hkv, Dv],
+ *            [B, Sq, Hq, Dv], [B, Hq, Sq] fp32 (lse may be NULL).  Page-locked (pinned) memory is
+ *            needed for the copies to overlap; pageable memory works but serialises them.
+ *   workspace: DEVICE scratch of sdpa_fwd_host_workspace_size(...) bytes, 16-byte aligned.
+ *   in_dtype = out_dtype: SDPA_F16 or SDPA_BF16.  Head dims, scale, causal: as in sdpa_fwd.
+ * Asynchronous: when the call returns, `stream` has been made to wait for the last copy back,
+ * so synchronizing `stream` makes o and lse readable.  The two copy streams and their events
+ * are created on the first call on a device (make that call outside stream capture) and kept
+ * until the process exits; concurrent calls on one device are serialised while they enqueue
+ * and share the copy streams.  On SDPA_ERR_CUDA part of the work may already be enqueued.
+ */
+int sdpa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,
+                  int Sk, int D, int Dv, float scale, int causal, void* workspace, size_t workspace_bytes,
+                  sdpa_dtype in_dtype, sdpa_dtype out_dtype, void* stream);
+
+/*
  * sdpa_fwd_int8_workspace_size -- bytes of device scratch sdpa_fwd_int8 needs: the 16-bit copies
  * of the int8 operands (Q and K, plus V when v_int8 != 0; B*S*H*D*2 bytes each, rounded up to 16)
  * followed by the optional split partials described under sdpa_fwd_workspace_size.  Sizes below
