@@ -415,9 +415,19 @@ int sdpa_fwd_int8(const void* q, const void* k, const void* v, void* o, float* l
   void* v16 = v_int8 ? static_cast<char*>(k16) + round16((size_t)B * Sk * Hkv * D * 2) : const_cast<void*>(v);
   Int8Args a{q_scale, k_scale, v_scale, WidenParams{}};
   a.widen.to_bf16 = out_dtype == SDPA_BF16;
-  a.widen.seg[0] = WidenSeg{static_cast<const int8_t*>(q), st[0], st[1], st[2], B, Sq, Hq, D, q16};
-  a.widen.seg[1] = WidenSeg{static_cast<const int8_t*>(k), st[3], st[4], st[5], B, Sk, Hkv, D, k16};
-  if (v_int8) a.widen.seg[2] = WidenSeg{static_cast<const int8_t*>(v), st[6], st[7], st[8], B, Sk, Hkv, D, v16};
+  auto seg = [&](const void* src, const int64_t* s3, int S, int H) {
+    const bool contig = s3[2] == D && s3[1] == (int64_t)H * D && s3[0] == (int64_t)S * H * D;
+    return WidenSeg{static_cast<const int8_t*>(src), s3[0], s3[1], s3[2], B, S, H, D, nullptr, contig ? 1 : 0};
+  };
+  if ((long long)B * std::max(Sq, Sk) * std::max(Hq, Hkv) >= (1ll << 31)) return SDPA_ERR_UNSUPPORTED;
+  a.widen.seg[0] = seg(q, st, Sq, Hq);
+  a.widen.seg[0].dst = q16;
+  a.widen.seg[1] = seg(k, st + 3, Sk, Hkv);
+  a.widen.seg[1].dst = k16;
+  if (v_int8) {
+    a.widen.seg[2] = seg(v, st + 6, Sk, Hkv);
+    a.widen.seg[2].dst = v16;
+  }
   a.widen.n_seg = v_int8 ? 3 : 2;
   // the prefill reads the contiguous copies; V keeps the caller's strides when it is 16-bit
   const int64_t st16[SDPA_FWD_NSTRIDES] = {(int64_t)Sq * Hq * D,

@@ -145,8 +145,9 @@ struct MaskConvertParams {
 struct WidenSeg {
   const int8_t* src;
   int64_t sb, ss, sh;
-  int B, S, H, Dh;         // Dh a multiple of 16
+  int B, S, H, Dh;         // Dh a multiple of 16; B * S * H < 2^31
   void* dst;               // [B, S, H, Dh] contiguous
+  int contig;              // the source is contiguous [B, S, H, Dh] too
 };
 struct WidenParams {
   WidenSeg seg[3];

@@ -108,3 +108,18 @@ def test_full_size_workload_sampled_rows():
     got_o, got_lse = gather_rows(o, lse, rows)
     assert_close(got_o, ref_o, TOL_16BIT)
     assert_lse_close(got_lse, ref_lse, TOL_LSE_F16)
+
+
+def test_int8_strided_codes_match_contiguous():
+    # q and int8 v as head-dim slices of wider rows: the widening reads them through their strides
+    x = workloads.int8_prefill(2, 4, 2, 300, 260, 128, v="i8", seed=21)
+    g = _gpu(x)
+    wide_q = torch.zeros((2, 300, 4, 192), dtype=torch.int8, device=DEV)
+    wide_q[..., 32:160] = g["q"]
+    wide_v = torch.zeros((2, 260, 2, 192), dtype=torch.int8, device=DEV)
+    wide_v[..., 64:192] = g["v"]
+    args = (g["q_scale"], g["k_scale"], g["v_scale"])
+    o1, l1 = fa.sdpa_fwd_int8(wide_q[..., 32:160], g["k"], wide_v[..., 64:192], *args, causal=True)
+    o2, l2 = fa.sdpa_fwd_int8(g["q"], g["k"], g["v"], *args, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
