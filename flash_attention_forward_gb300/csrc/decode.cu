@@ -340,16 +340,34 @@ __global__ void __launch_bounds__(kDecodeDv) decode_combine_kernel(const DecodeP
   const int h = blockIdx.x, b = blockIdx.y, dv = threadIdx.x;
   const int L = min(max(__ldg(p.kv_len + b), 0), p.max_kv);
   const int ns = (L + kDecodeSplit - 1) / kDecodeSplit;
-  const float* base = p.ws + (int64_t)(b * p.Hq + h) * p.n_splits_max * (kDecodeDv + 2);
+  constexpr int kPart = kDecodeDv + 2;  // floats per partial: O, then max, then sum
+  constexpr int kGroup = 8;             // partials whose loads are in flight together
+  const float* base = p.ws + (int64_t)(b * p.Hq + h) * p.n_splits_max * kPart;
   float M = -INFINITY;
-  for (int s = 0; s < ns; ++s) M = fmaxf(M, base[s * (kDecodeDv + 2) + kDecodeDv]);
+  for (int s0 = 0; s0 < ns; s0 += kGroup) {
+    float m[kGroup];
+#pragma unroll
+    for (int i = 0; i < kGroup; ++i) m[i] = (s0 + i < ns) ? __ldg(base + (s0 + i) * kPart + kDecodeDv) : -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kGroup; ++i) M = fmaxf(M, m[i]);
+  }
   float o = 0.f, ls = 0.f;
-  for (int s = 0; s < ns; ++s) {
-    const float* part = base + s * (kDecodeDv + 2);
-    const float ms = part[kDecodeDv];
-    const float e = (ms == -INFINITY) ? 0.f : ex2(ms - M);
-    o += e * part[dv];
-    ls += e * part[kDecodeDv + 1];
+  for (int s0 = 0; s0 < ns; s0 += kGroup) {
+    float m[kGroup], x[kGroup], l[kGroup];
+#pragma unroll
+    for (int i = 0; i < kGroup; ++i) {
+      const bool in = s0 + i < ns;
+      const float* part = base + (s0 + i) * kPart;
+      m[i] = in ? __ldg(part + kDecodeDv) : -INFINITY;
+      x[i] = in ? __ldg(part + dv) : 0.f;
+      l[i] = in ? __ldg(part + kDecodeDv + 1) : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < kGroup; ++i) {  // splits in order, as a sequential loop would take them
+      const float e = (m[i] == -INFINITY) ? 0.f : ex2(m[i] - M);
+      o += e * x[i];
+      ls += e * l[i];
+    }
   }
   const float out = ls > 0.f ? o / ls : 0.f;
   uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + b * p.o_b + (int64_t)h * p.o_h;
