@@ -56,3 +56,36 @@ def test_decode_graph_replays_match_eager():
         torch.cuda.synchronize()
         assert torch.equal(o, ro) and torch.equal(lse, rl)
     assert fa.sdpa_check_device_status() == fa.SDPA_OK
+
+
+def test_varlen_and_int8_graph_replays_match_eager():
+    seq = [300, 5, 640]
+    vx = workloads.varlen_pack(seq, seq, 4, 2, 128, 128, dtype="bf16", seed=8)
+    q, k, v, cu_q, cu_k = (vx[n].to(DEV) for n in ("q", "k", "v", "cu_q", "cu_k"))
+    ix = {n: (None if t is None else t.to(DEV))
+          for n, t in workloads.int8_prefill(1, 4, 2, 500, 700, 128, v="i8", seed=9).items()}
+    vo = torch.empty((q.shape[0], 4, 128), dtype=torch.bfloat16, device=DEV)
+    vws = torch.empty(fa.sdpa_fwd_varlen_workspace_size(len(seq)), dtype=torch.uint8, device=DEV)
+    io = torch.empty((1, 500, 4, 128), dtype=torch.float16, device=DEV)
+    iws = torch.empty(fa.sdpa_fwd_int8_workspace_size(1, 4, 2, 500, 700, 128, True, True), dtype=torch.uint8,
+                      device=DEV)
+    iargs = (ix["q"], ix["k"], ix["v"], ix["q_scale"], ix["k_scale"], ix["v_scale"])
+
+    def calls():
+        fa.sdpa_fwd_varlen(q, k, v, cu_q, cu_k, max(seq), causal=True, out=vo, return_lse=False, workspace=vws)
+        fa.sdpa_fwd_int8(*iargs, causal=True, out=io, return_lse=False, workspace=iws)
+
+    calls()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        calls()
+    for r in range(2):
+        q.mul_(-1.0), ix["q"].neg_()  # new inputs in the static buffers
+        g.replay()
+        torch.cuda.synchronize()
+        rv, _ = fa.sdpa_fwd_varlen(q, k, v, cu_q, cu_k, max(seq), causal=True)
+        ri, _ = fa.sdpa_fwd_int8(*iargs, causal=True)
+        torch.cuda.synchronize()
+        assert torch.equal(vo[: int(cu_q[-1])], rv[: int(cu_q[-1])]) and torch.equal(io, ri)
+    assert fa.sdpa_check_device_status() == fa.SDPA_OK
