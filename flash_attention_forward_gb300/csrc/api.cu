@@ -461,12 +461,21 @@ std::mutex g_pipe_mu;  // held while a call enqueues (the events are shared)
 
 cudaError_t host_pipe(int dev, HostPipe** out) {
   HostPipe& hp = g_pipe[dev];
-  cudaError_t e;
   if (hp.h2d == nullptr) {
-    if ((e = cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking)) != cudaSuccess) return e;
-    if ((e = cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking)) != cudaSuccess) return e;
-    for (cudaEvent_t& ev : hp.ev)
-      if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess) return e;
+    // build the whole set first: a failure part-way leaves the device's entry empty
+    HostPipe fresh;
+    cudaError_t e = cudaStreamCreateWithFlags(&fresh.h2d, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&fresh.d2h, cudaStreamNonBlocking);
+    for (cudaEvent_t& ev : fresh.ev)
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      for (cudaEvent_t ev : fresh.ev)
+        if (ev) cudaEventDestroy(ev);
+      if (fresh.d2h) cudaStreamDestroy(fresh.d2h);
+      if (fresh.h2d) cudaStreamDestroy(fresh.h2d);
+      return e;
+    }
+    hp = fresh;
   }
   *out = &hp;
   return cudaSuccess;
