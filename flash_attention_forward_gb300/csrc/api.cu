@@ -561,7 +561,10 @@ int sdpa_fwd_host(const void* q, const void* k, const void* v, void* o, float* l
   if (cudaMemcpyAsync(dk, k, (size_t)B * Sk * krow, cudaMemcpyHostToDevice, hp->h2d) != cudaSuccess ||
       cudaMemcpyAsync(dv, v, (size_t)B * Sk * vrow, cudaMemcpyHostToDevice, hp->h2d) != cudaSuccess)
     return SDPA_ERR_CUDA;
-  for (int c = 0; c < n_chunks; ++c) {
+  for (int i = 0; i < n_chunks; ++i) {
+    // causal: the last rows first.  Their chunk is the longest to compute, so it now overlaps
+    // the later uploads, and the pipeline ends on the cheapest chunk.
+    const int c = causal ? n_chunks - 1 - i : i;
     const int r0 = c * rows, r1 = std::min(Sq, r0 + rows);
     // causal (top-left): rows r0..r1-1 see keys below r1; otherwise every key
     const int k_need = causal ? std::min(Sk, r1) : Sk;

@@ -185,8 +185,9 @@ size_t sdpa_fwd_host_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int 
 /*
  * sdpa_fwd_host -- sdpa_fwd on HOST buffers: copies the inputs to the device, computes, and
  * copies O (and LSE) back, overlapping the three.  K and V go up first on a copy stream, then
- * Q in at most 8 chunks of whole 256-row work tiles; chunk c's prefill runs in `stream` as soon
- * as its rows have landed (over the keys those rows see, causal masking counted from the
+ * Q in at most 8 chunks of whole 256-row work tiles (causal: the last rows first, so that the
+ * most expensive chunk overlaps the remaining uploads); a chunk's prefill runs in `stream` as
+ * soon as its rows have landed (over the keys those rows see, causal masking counted from the
  * chunk's global row), and its O rows come back on a second copy stream while later chunks are
  * still copying or computing.  Results equal sdpa_fwd's on the same inputs (causal: bit for bit).
  *
