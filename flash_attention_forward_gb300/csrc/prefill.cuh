@@ -271,6 +271,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   using C = PrefillCfg<ELEM, D, DV>;
   constexpr bool VARLEN = VAR == kVarlen;
   constexpr bool SCALED = VAR == kBlockScaled;
+  // 16-bit ring without a mask: tile 0's softmax waits for ring step j+1 before it signals P_0(j),
+  // which spares the MMA thread that wait (with a mask the longer softmax would then hold it up)
+  constexpr bool T0_COVERS_STEP = ELEM != kE4M3 && !MASK;
   constexpr int ST = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -448,7 +451,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
               break;
             }
           } else {
-            if (!mbar_wait(&in_full[s], r & 1, abort_flag, p.status)) {
+            // A step that starts with P_0(j-1) V(j-1) needs no wait of its own: tile 0's softmax
+            // saw this stage land before it signalled P_0(j-1).
+            const bool covered = T0_COVERS_STEP && j >= 1 && j - 1 < w.n_t[0];
+            if (!covered && !mbar_wait(&in_full[s], r & 1, abort_flag, p.status)) {
               ok = false;
               break;
             }
@@ -562,11 +568,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const uint32_t tS = tmem_base + lane_off + t * 128;
     const uint32_t tO = tmem_base + lane_off + 256 + t * 128;
     const float scale2 = p.scale2;
-    int sn = 0;  // S blocks consumed (s_full / p_full phases)
-    int on = 0;  // work tiles finished (o_full phases)
+    int sn = 0;     // S blocks consumed (s_full / p_full phases)
+    int on = 0;     // work tiles finished (o_full phases)
+    int gbase = 0;  // 16-bit ring: ring step of the current work tile's step 0 (tile 0 uses it)
     bool ok = true;
     for (int k = 0, item = nth_item(0); ok && item < n_items; item = nth_item(++k)) {
       const WorkTile w = work_tile<CAUSAL, VARLEN>(p, item);
+      const int g0 = gbase;
+      gbase += w.n_blocks > 0 ? w.n_blocks + 1 : 0;  // every role skips empty units
       const int n = w.n_t[t];
       if (n == 0) continue;
       const int qrow = w.q0 + t * kBlockQ + row;
@@ -709,6 +718,16 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
               o[i + 1] = __float_as_uint(b);
             }
             tmem_st32(tO + c * 32, o);
+          }
+        }
+        // P_0(j) also stands for ring step j+1 having landed, so the MMA thread skips its own wait
+        // at that step.  Tile 0 is active in every work tile, and the MMA thread waits for itself
+        // at every step tile 0 does not cover, so this wait never falls two phases behind.
+        if (T0_COVERS_STEP && t == 0) {
+          const int g_next = g0 + j + 1;
+          if (!mbar_wait_warp(&in_full[g_next % ST], (g_next / ST) & 1, abort_flag, p.status)) {
+            ok = false;
+            break;
           }
         }
         tmem_st_wait();
