@@ -271,9 +271,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   using C = PrefillCfg<ELEM, D, DV>;
   constexpr bool VARLEN = VAR == kVarlen;
   constexpr bool SCALED = VAR == kBlockScaled;
-  // 16-bit ring without a mask: tile 0's softmax waits for ring step j+1 before it signals P_0(j),
-  // which spares the MMA thread that wait (with a mask the longer softmax would then hold it up)
-  constexpr bool T0_COVERS_STEP = ELEM != kE4M3 && !MASK;
+  // Without a mask, tile 0's softmax waits for what the MMA thread's step j+1 reads before it
+  // signals P_0(j) (16-bit: ring step j+1 landed; e4m3: V(j) converted and K(j+1) landed), which
+  // spares the MMA thread those waits (with a mask the longer softmax would then hold it up)
+  constexpr bool T0_COVERS_STEP = !MASK;
   constexpr int ST = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -444,16 +445,17 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           const int gv = (ELEM == kE4M3) ? g + j - 1 : g;        // stage of V(j-1)
           const int s = gk % ST, r = gk / ST;
           const int sv = gv % ST, rv = gv / ST;
-          bool k_ready = ELEM != kE4M3;  // e4m3: K(j) is waited for just before the first QK
+          // e4m3: K(j) is waited for just before the first QK, unless tile 0's softmax covered it
+          const bool covered = T0_COVERS_STEP && j >= 1 && j - 1 < w.n_t[0];
+          bool k_ready = ELEM != kE4M3 || covered;
           if constexpr (ELEM == kE4M3) {
-            if (j >= 1 && !mbar_wait(&v_ready[sv], rv & 1, abort_flag, p.status)) {
+            if (j >= 1 && !covered && !mbar_wait(&v_ready[sv], rv & 1, abort_flag, p.status)) {
               ok = false;
               break;
             }
           } else {
             // A step that starts with P_0(j-1) V(j-1) needs no wait of its own: tile 0's softmax
             // saw this stage land before it signalled P_0(j-1).
-            const bool covered = T0_COVERS_STEP && j >= 1 && j - 1 < w.n_t[0];
             if (!covered && !mbar_wait(&in_full[s], r & 1, abort_flag, p.status)) {
               ok = false;
               break;
@@ -570,12 +572,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const float scale2 = p.scale2;
     int sn = 0;     // S blocks consumed (s_full / p_full phases)
     int on = 0;     // work tiles finished (o_full phases)
-    int gbase = 0;  // 16-bit ring: ring step of the current work tile's step 0 (tile 0 uses it)
+    int gbase = 0;  // ring index of the current work tile's first step (tile 0 uses it)
     bool ok = true;
     for (int k = 0, item = nth_item(0); ok && item < n_items; item = nth_item(++k)) {
       const WorkTile w = work_tile<CAUSAL, VARLEN>(p, item);
       const int g0 = gbase;
-      gbase += w.n_blocks > 0 ? w.n_blocks + 1 : 0;  // every role skips empty units
+      // every role skips empty units; the 16-bit ring takes n_blocks + 1 steps, e4m3 n_blocks
+      gbase += w.n_blocks > 0 ? w.n_blocks + (ELEM == kE4M3 ? 0 : 1) : 0;
       const int n = w.n_t[t];
       if (n == 0) continue;
       const int qrow = w.q0 + t * kBlockQ + row;
@@ -720,14 +723,24 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             tmem_st32(tO + c * 32, o);
           }
         }
-        // P_0(j) also stands for ring step j+1 having landed, so the MMA thread skips its own wait
+        // P_0(j) also stands for what the MMA thread's step j+1 reads, so it skips its own waits
         // at that step.  Tile 0 is active in every work tile, and the MMA thread waits for itself
-        // at every step tile 0 does not cover, so this wait never falls two phases behind.
+        // at every step tile 0 does not cover, so these waits never fall two phases behind.
         if (T0_COVERS_STEP && t == 0) {
-          const int g_next = g0 + j + 1;
-          if (!mbar_wait_warp(&in_full[g_next % ST], (g_next / ST) & 1, abort_flag, p.status)) {
-            ok = false;
-            break;
+          if constexpr (ELEM == kE4M3) {
+            const int gv = g0 + j;  // V(j) converted; K(j+1) landed when there is a block j+1
+            if (!mbar_wait_warp(&v_ready[gv % ST], (gv / ST) & 1, abort_flag, p.status) ||
+                (j + 1 < w.n_blocks &&
+                 !mbar_wait_warp(&in_full[(gv + 1) % ST], ((gv + 1) / ST) & 1, abort_flag, p.status))) {
+              ok = false;
+              break;
+            }
+          } else {
+            const int g_next = g0 + j + 1;
+            if (!mbar_wait_warp(&in_full[g_next % ST], (g_next / ST) & 1, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
           }
         }
         tmem_st_wait();

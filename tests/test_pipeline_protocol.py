@@ -162,3 +162,145 @@ def test_protocol_has_no_alias_or_deadlock(stages):
 def test_model_catches_a_tile_waiting_on_a_barrier_nobody_waits_for():
     failures = [_run(_random_units(random.Random(s)), 2, s, tile1_on_released=True) for s in range(300)]
     assert sum(f is not None for f in failures) > 50
+
+
+def _run_e4m3(units, stages, seed, t0_covers=True):
+    """The e4m3 ring: K(j) and raw V(j) load one step ahead of P.V(j); two converter warps turn
+    raw V into f16 (v_ready).  With t0_covers, tile 0's softmax waits for V(j-1) converted and K(j)
+    landed before it signals P_0(j-1), and the MMA thread skips both waits at that step."""
+    rnd = random.Random(seed)
+    bars = {}
+
+    def bar(name):
+        return bars.setdefault(name, _Bar(name))
+
+    def producer():
+        g, qn = 0, [0, 0]
+        for nt in units:
+            nb = max(nt)
+            if nb == 0:
+                continue
+            for t in range(2):
+                if nt[t] == 0:
+                    continue
+                if qn[t] > 0:
+                    yield ("wait", bar(f"q_empty{t}"), qn[t] - 1)
+                yield ("do", bar(f"q_full{t}"))
+                qn[t] += 1
+            for _ in range(nb):
+                s, r = g % stages, g // stages
+                if r > 0:
+                    yield ("wait", bar(f"released{s}"), r - 1)
+                yield ("do", bar(f"in_full{s}"))
+                if r > 0:
+                    yield ("wait", bar(f"v_free{s}"), r - 1)
+                yield ("do", bar(f"v_full{s}"))
+                g += 1
+
+    def converter():
+        g = 0
+        for nt in units:
+            for _ in range(max(nt)):
+                s, r = g % stages, g // stages
+                yield ("wait", bar(f"v_full{s}"), r)
+                yield ("do", bar(f"v_ready{s}"))
+                g += 1
+
+    def mma():
+        g, qn, pn = 0, [0, 0], [0, 0]
+        for nt in units:
+            nb = max(nt)
+            if nb == 0:
+                continue
+            for t in range(2):
+                if nt[t] > 0:
+                    yield ("wait", bar(f"q_full{t}"), qn[t])
+            for j in range(nb + 1):
+                gk, gv = g + j, g + j - 1
+                covered = t0_covers and j >= 1 and j - 1 < nt[0]
+                if j >= 1 and not covered:
+                    yield ("wait", bar(f"v_ready{gv % stages}"), gv // stages)
+                k_ready = covered
+                for t in range(2):
+                    if j >= 1 and j - 1 < nt[t]:
+                        if j == 1 and qn[t] > 0:
+                            yield ("wait", bar(f"o_empty{t}"), qn[t] - 1)
+                        yield ("wait", bar(f"p_full{t}"), pn[t])
+                        pn[t] += 1
+                        if j == nt[t]:
+                            yield ("do", bar(f"o_full{t}"))
+                    if t == 1 and j >= 1:
+                        yield ("do", bar(f"v_free{gv % stages}"))
+                    if j < nt[t]:
+                        if not k_ready:
+                            yield ("wait", bar(f"in_full{gk % stages}"), gk // stages)
+                            k_ready = True
+                        yield ("do", bar(f"s_full{t}"))
+                        if j == nt[t] - 1:
+                            yield ("do", bar(f"q_empty{t}"))
+                if j < nb:
+                    yield ("do", bar(f"released{gk % stages}"))
+            g += nb
+            for t in range(2):
+                if nt[t] > 0:
+                    qn[t] += 1
+
+    def softmax(t):
+        sn = on = gbase = 0
+        for nt in units:
+            nb = max(nt)
+            g0 = gbase
+            gbase += nb
+            if nt[t] == 0:
+                continue
+            for j in range(nt[t]):
+                yield ("wait", bar(f"s_full{t}"), sn)
+                if t == 0 and t0_covers:
+                    G = g0 + j
+                    yield ("wait", bar(f"v_ready{G % stages}"), G // stages)
+                    if j + 1 < nb:
+                        yield ("wait", bar(f"in_full{(G + 1) % stages}"), (G + 1) // stages)
+                yield ("do", bar(f"p_full{t}"))
+                sn += 1
+            yield ("wait", bar(f"o_full{t}"), on)
+            on += 1
+            yield ("do", bar(f"o_empty{t}"))
+
+    roles = {"producer": producer(), "converter": converter(), "mma": mma(), "softmax0": softmax(0),
+             "softmax1": softmax(1)}
+    pending = {}
+    for name, gen in roles.items():
+        op = next(gen, None)
+        if op is not None:
+            pending[name] = op
+    while pending:
+        ready = []
+        for name, op in pending.items():
+            if op[0] == "do":
+                ready.append(name)
+                continue
+            b, index = op[1], op[2]
+            if (b.phase & 1) != (index & 1):
+                if b.phase < index + 1:
+                    return f"alias: {name} passed {b.name} phase {index} at phase {b.phase}"
+                ready.append(name)
+        if not ready:
+            return "deadlock: " + ", ".join(f"{n} on {op[1].name}" for n, op in pending.items())
+        name = rnd.choice(ready)
+        op = pending[name]
+        if op[0] == "do":
+            op[1].arrive()
+        nxt = next(roles[name], None)
+        if nxt is None:
+            del pending[name]
+        else:
+            pending[name] = nxt
+    return None
+
+
+@pytest.mark.parametrize("t0_covers", [False, True])
+@pytest.mark.parametrize("stages", [2, 4])
+def test_e4m3_protocol_has_no_alias_or_deadlock(stages, t0_covers):
+    for seed in range(1000):
+        units = _random_units(random.Random(seed))
+        assert _run_e4m3(units, stages, seed, t0_covers=t0_covers) is None, units
