@@ -256,7 +256,8 @@ __device__ __forceinline__ int nth_item(int k) {
 //   e4m3 inputs, where V(j) must also be converted to f16 before P V(j), K(j) and V(j) load
 //   together one step ahead of their P.V:
 //   in_full[s] / released[s]: K(j) landed / its QK MMAs finished
-//   v_full[s] / v_free[s]   : raw V(j) landed / P V(j) finished (raw and converted V free)
+//   v_full[s] / vraw_free[s]: raw V(j) landed / raw V(j) read by the converter (raw buffer free)
+//   v_free[s]               : P V(j) finished (converted buffer free)
 //   v_ready[s]              : V(j) converted to f16
 //   s_full[t]               : S_t = Q_t K^T finished
 //   p_full[t]               : P_t written to tensor memory (and O_t rescaled if needed)
@@ -290,7 +291,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   uint64_t* v_full = released + ST;        // [ST] e4m3: raw V(j) landed
   uint64_t* v_free = v_full + ST;          // [ST] e4m3: V stage (raw and converted) free
   uint64_t* v_ready = v_free + ST;         // [ST] e4m3: V(j) converted to f16
-  uint64_t* s_full = v_ready + ST;         // [2]
+  uint64_t* vraw_free = v_ready + ST;      // [ST] e4m3: raw V(j) converted (raw buffer free)
+  uint64_t* s_full = vraw_free + ST;       // [2]
   uint64_t* p_full = s_full + 2;           // [2]
   uint64_t* o_full = p_full + 2;           // [2]
   uint64_t* o_empty = o_full + 2;          // [2]
@@ -318,6 +320,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       mbar_init(&v_full[s], 1);
       mbar_init(&v_free[s], 1);
       mbar_init(&v_ready[s], 64);
+      mbar_init(&vraw_free[s], 64);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -370,7 +373,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             for (int c = 0; c < C::NCH_D; ++c)
               tma_load_4d(sK + s * C::K_BYTES + c * kBlockK * C::CHB, &tm_k, &in_full[s], c * C::CH, w.kvh,
                           w.k_off + (w.jb0 + j) * kBlockK, w.cb);
-            if (r > 0 && !mbar_wait(&v_free[s], (r - 1) & 1, abort_flag, p.status)) {
+            // the raw buffer frees as soon as the converter has read it
+            if (r > 0 && !mbar_wait(&vraw_free[s], (r - 1) & 1, abort_flag, p.status)) {
               ok = false;
               break;
             }
@@ -544,6 +548,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             ok = false;
             break;
           }
+          // the converted buffer of this stage is free once the previous P.V that read it finished
+          if (r > 0 && !mbar_wait(&v_free[s], (r - 1) & 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
           const uint8_t* src = sVraw + s * C::VRAW_BYTES;
           uint8_t* dst = sV + s * C::V_BYTES;
           constexpr int UNITS = kBlockK * DV / 8;  // 8 values per unit
@@ -557,6 +566,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           }
           fence_proxy_async_smem();
           mbar_arrive(&v_ready[s]);
+          mbar_arrive(&vraw_free[s]);
         }
       }
     }

@@ -166,8 +166,10 @@ def test_model_catches_a_tile_waiting_on_a_barrier_nobody_waits_for():
 
 def _run_e4m3(units, stages, seed, t0_covers=True):
     """The e4m3 ring: K(j) and raw V(j) load one step ahead of P.V(j); two converter warps turn
-    raw V into f16 (v_ready).  With t0_covers, tile 0's softmax waits for V(j-1) converted and K(j)
-    landed before it signals P_0(j-1), and the MMA thread skips both waits at that step."""
+    raw V into f16 (v_ready), free the raw buffer themselves (vraw_free) and write the converted
+    buffer only after the P.V that last read it (v_free).  With t0_covers, tile 0's softmax waits
+    for V(j-1) converted and K(j) landed before it signals P_0(j-1), and the MMA thread skips both
+    waits at that step."""
     rnd = random.Random(seed)
     bars = {}
 
@@ -193,7 +195,7 @@ def _run_e4m3(units, stages, seed, t0_covers=True):
                     yield ("wait", bar(f"released{s}"), r - 1)
                 yield ("do", bar(f"in_full{s}"))
                 if r > 0:
-                    yield ("wait", bar(f"v_free{s}"), r - 1)
+                    yield ("wait", bar(f"vraw_free{s}"), r - 1)
                 yield ("do", bar(f"v_full{s}"))
                 g += 1
 
@@ -203,7 +205,10 @@ def _run_e4m3(units, stages, seed, t0_covers=True):
             for _ in range(max(nt)):
                 s, r = g % stages, g // stages
                 yield ("wait", bar(f"v_full{s}"), r)
+                if r > 0:
+                    yield ("wait", bar(f"v_free{s}"), r - 1)
                 yield ("do", bar(f"v_ready{s}"))
+                yield ("do", bar(f"vraw_free{s}"))
                 g += 1
 
     def mma():
