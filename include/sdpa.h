@@ -345,7 +345,7 @@ int sdpa_version(void);
 
 /*
  * sdpa_debug_stall_next_call -- test hook for the failure path.  Arms a one-shot flag
- * (process-wide): the next sdpa_fwd / sdpa_fwd_fp8 launch withholds its first K/V stage, so
+ * (process-wide): the next prefill launch (of any sdpa_fwd* entry point) withholds its first K/V stage, so
  * every CTA's bounded waits give up after about one second, the CTAs drain their copies,
  * free tensor memory and exit, and sdpa_check_device_status() then returns
  * SDPA_ERR_TIMEOUT.  The CUDA context stays usable.  Returns SDPA_OK.  Nothing in the
