@@ -387,6 +387,9 @@ __global__ void __launch_bounds__(kDecodeDv) decode_combine_kernel(const DecodeP
 constexpr int kMaskGroup = 4;
 
 __global__ void __launch_bounds__(128) mask_convert_kernel(const MaskConvertParams p) {
+  // the prefill that reads the bits may be scheduled as soon as every CTA here has started; it
+  // waits for this grid's completion before its first read of them
+  pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_groups = (p.n_kblocks + kMaskGroup - 1) / kMaskGroup;
   const int64_t item = (int64_t)blockIdx.x * 4 + warp;

@@ -304,6 +304,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int n_items = p.n_units;
+  // the split merge, if any, may be scheduled early (it waits for this grid's completion)
+  if constexpr (!CAUSAL && !VARLEN) pdl_launch_dependents();
 
   if (tid == 0) {
     for (int t = 0; t < 2; ++t) {
@@ -573,6 +575,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   } else {
     // ------------------------------------------------------------ softmax warpgroups
     regs_inc<kRegsSoftmax>();
+    if constexpr (MASK) pdl_wait();  // the condensed mask comes from the kernel launched before
     const int t = (warp - 4) >> 2;           // query tile slot of this warpgroup
     const int wq = warp & 3;                 // tensor-memory lane quarter
     const int row = wq * 32 + lane;          // row within the tile
@@ -849,6 +852,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 template <int ELEM, int DV>
 __global__ void __launch_bounds__(128) split_combine_kernel(const PrefillParams p) {
   constexpr int kChunks = DV / 8;
+  pdl_wait();  // the partials come from the prefill launched before
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<long long>(p.split_tail) * kCtaRows * kChunks) return;
   const int chunk = static_cast<int>(idx % kChunks);

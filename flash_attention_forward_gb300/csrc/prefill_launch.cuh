@@ -32,11 +32,35 @@ cudaError_t launch_prefill_instance(const CUtensorMap& tq, const CUtensorMap& tk
   long long ug = aligned < cap ? aligned : cap;
   const long long kv_units = (long long)p.B * p.Hkv;
   q.units_per_group = (int)(ug < 1 ? 1 : (ug > kv_units ? kv_units : ug));
-  kern<<<grid, kPrefillThreads, C::SMEM, st>>>(tq, tk, tv, q);
-  if (!CAUSAL && VAR != kVarlen && p.split_parts > 1) {
+  // Programmatic dependent launch where the previous kernel of the stream is this library's own:
+  // the masked prefill after mask_convert_kernel (only its softmax reads what that kernel
+  // writes, after griddepcontrol.wait), and the split merge after the prefill.
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  if constexpr (MASK) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kPrefillThreads);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = st;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    if ((e = cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, q)) != cudaSuccess) return e;
+  } else {
+    kern<<<grid, kPrefillThreads, C::SMEM, st>>>(tq, tk, tv, q);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (!CAUSAL && VAR != kVarlen && p.split_parts > 1) {
     const long long threads = (long long)p.split_tail * kCtaRows * (DV / 8);
-    split_combine_kernel<ELEM == kE4M3 ? kBF16 : ELEM, DV><<<(unsigned)((threads + 127) / 128), 128, 0, st>>>(q);
+    cudaLaunchConfig_t ccfg = {};
+    ccfg.gridDim = dim3((unsigned)((threads + 127) / 128));
+    ccfg.blockDim = dim3(128);
+    ccfg.stream = st;
+    ccfg.attrs = pdl;
+    ccfg.numAttrs = 1;
+    if ((e = cudaLaunchKernelEx(&ccfg, split_combine_kernel<ELEM == kE4M3 ? kBF16 : ELEM, DV>, q)) != cudaSuccess)
+      return e;
   }
   return cudaGetLastError();
 }

@@ -96,6 +96,13 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
 
 // ---------------------------------------------------------------- fences
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel of the stream, if it was
+// launched to allow it, be scheduled once every CTA of this grid has issued it; wait blocks until
+// the previous kernel of the stream has completed and its writes are visible.  Both are no-ops
+// for launches that did not opt in.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
