@@ -97,3 +97,74 @@ def test_fp8_and_decode_validation_codes(lib):
     assert dec(Hq=32, Hkv=2) == fa.SDPA_ERR_UNSUPPORTED  # group of 16
     assert dec(dt=fa.SDPA_E4M3) == fa.SDPA_ERR_UNSUPPORTED
     assert dec(max_kv=0) == fa.SDPA_ERR_INVALID
+
+
+def test_new_entry_points_are_declared(lib):
+    names = set(fa.declared_functions())
+    assert {"sdpa_fwd_varlen", "sdpa_fwd_varlen_fp8", "sdpa_fwd_varlen_workspace_size", "sdpa_fwd_int8",
+            "sdpa_fwd_int8_workspace_size", "sdpa_fwd_host", "sdpa_fwd_host_workspace_size",
+            "sdpa_decode_paged", "sdpa_decode_noalloc"} <= names
+
+
+def test_new_workspace_sizes(lib):
+    # packed sequences: the int32 tile prefix [B + 1], rounded up to 16 bytes
+    assert fa.sdpa_fwd_varlen_workspace_size(1) == 16
+    assert fa.sdpa_fwd_varlen_workspace_size(16) == 80
+    assert fa.sdpa_fwd_varlen_workspace_size(0) == 0
+    # int8 codes: 16-bit copies of Q and K (and V when int8); no device here, so no split part
+    q, kv = 2 * 4096 * 32 * 128 * 2, 2 * 4096 * 8 * 128 * 2
+    assert fa.sdpa_fwd_int8_workspace_size(2, 32, 8, 4096, 4096, 128, False, True) == q + kv
+    assert fa.sdpa_fwd_int8_workspace_size(2, 32, 8, 4096, 4096, 128, True, True) == q + 2 * kv
+    # host-buffer call: device copies of Q, K, V, O and LSE
+    lse = 2 * 32 * 4096 * 4
+    assert fa.sdpa_fwd_host_workspace_size(2, 32, 8, 4096, 4096, 128, 128, True) == q + 2 * kv + q + lse
+
+
+def test_varlen_int8_and_host_validation_codes(lib):
+    f, sz = ctypes.c_float, ctypes.c_size_t
+
+    def varlen(**over):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, cq=FAKE, ck=FAKE, B=2, Hq=4, Hkv=2, tq=100, tk=100,
+                 maxq=60, D=128, Dv=128, strides=None, scale=f(0.1), causal=1, ws=FAKE, wsb=sz(1 << 10),
+                 dt=fa.SDPA_BF16, odt=fa.SDPA_BF16, stream=None)
+        a.update(over)
+        return lib.sdpa_fwd_varlen(*a.values())
+
+    assert varlen(B=0) == fa.SDPA_ERR_INVALID
+    assert varlen(tk=0) == fa.SDPA_ERR_INVALID
+    assert varlen(maxq=101) == fa.SDPA_ERR_INVALID     # longer than all the packed rows
+    assert varlen(cq=None) == fa.SDPA_ERR_INVALID
+    assert varlen(ck=ctypes.c_void_p(0x10002)) == fa.SDPA_ERR_INVALID  # offsets must be 4-byte aligned
+    assert varlen(ws=None) == fa.SDPA_ERR_INVALID
+    assert varlen(wsb=sz(8)) == fa.SDPA_ERR_INVALID      # below the tile prefix size
+    assert varlen(dt=fa.SDPA_E4M3) == fa.SDPA_ERR_UNSUPPORTED
+    assert varlen(D=96, Dv=96) == fa.SDPA_ERR_UNSUPPORTED
+
+    def int8(**over):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, B=1, Hq=4, Hkv=2, Sq=64, Sk=64, D=128, strides=None,
+                 qs=FAKE, ks=FAKE, vs=None, scale=f(0.1), causal=1, ws=FAKE, wsb=sz(1 << 24),
+                 vdt=fa.SDPA_F16, odt=fa.SDPA_F16, stream=None)
+        a.update(over)
+        return lib.sdpa_fwd_int8(*a.values())
+
+    assert int8(qs=None) == fa.SDPA_ERR_INVALID
+    assert int8(vs=FAKE) == fa.SDPA_ERR_INVALID           # 16-bit V takes no channel scales
+    assert int8(vdt=fa.SDPA_I8) == fa.SDPA_ERR_INVALID    # int8 V needs them
+    assert int8(vdt=fa.SDPA_BF16) == fa.SDPA_ERR_UNSUPPORTED  # V values in another type than O
+    assert int8(odt=fa.SDPA_E4M3, vdt=fa.SDPA_E4M3) == fa.SDPA_ERR_UNSUPPORTED
+    assert int8(D=192) == fa.SDPA_ERR_UNSUPPORTED         # head dims 64 and 128 only
+    assert int8(wsb=sz(16)) == fa.SDPA_ERR_INVALID        # below the 16-bit copies
+    assert int8(ks=ctypes.c_void_p(0x10002)) == fa.SDPA_ERR_INVALID
+
+    def host(**over):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, B=1, Hq=4, Hkv=2, Sq=64, Sk=64, D=128, Dv=128,
+                 scale=f(0.1), causal=1, ws=FAKE, wsb=sz(1 << 24), dt=fa.SDPA_BF16, odt=fa.SDPA_BF16, stream=None)
+        a.update(over)
+        return lib.sdpa_fwd_host(*a.values())
+
+    assert host(q=None) == fa.SDPA_ERR_INVALID
+    assert host(Hkv=3) == fa.SDPA_ERR_INVALID
+    assert host(wsb=sz(1024)) == fa.SDPA_ERR_INVALID
+    assert host(odt=fa.SDPA_F16) == fa.SDPA_ERR_UNSUPPORTED
+    assert host(dt=fa.SDPA_E4M3, odt=fa.SDPA_E4M3) == fa.SDPA_ERR_UNSUPPORTED
+    assert host(D=96, Dv=96) == fa.SDPA_ERR_UNSUPPORTED
