@@ -417,3 +417,37 @@ def test_int8_quantization_recipe():
     vc, vs = workloads.quantize_int8_channels(x)
     assert vs.shape == (2, 3, 16)
     assert bool(((vc.double() * vs.double().unsqueeze(1) - x.double()).abs() <= vs.double().unsqueeze(1) / 2 + 1e-12).all())
+
+
+def test_key_split_recombines_exactly():
+    # attention over all keys = the log-sum-exp merge of attention over two disjoint key ranges
+    # (the algebra both split paths of the library rely on), to fp64 rounding
+    B, Sq, Sk, Hq, Hkv, D = 1, 7, 40, 2, 1, 16
+    q, k, v = _rand((B, Sq, Hq, D), 61), _rand((B, Sk, Hkv, D), 62), _rand((B, Sk, Hkv, D), 63)
+    o, lse = oracle.sdpa_fwd(q, k, v, scale=0.6)
+    o1, l1 = oracle.sdpa_fwd(q, k[:, :13], v[:, :13], scale=0.6)
+    o2, l2 = oracle.sdpa_fwd(q, k[:, 13:], v[:, 13:], scale=0.6)
+    m = np.maximum(l1, l2)
+    lse_merged = m + np.log(np.exp(l1 - m) + np.exp(l2 - m))
+    assert np.abs(lse_merged - lse).max() <= 1e-12
+    w1 = np.exp(l1 - lse).transpose(0, 2, 1)[..., None]  # [B, Sq, Hq, 1]
+    w2 = np.exp(l2 - lse).transpose(0, 2, 1)[..., None]
+    assert np.abs(w1 * o1 + w2 * o2 - o).max() <= 1e-12
+
+
+def test_scale_moves_between_q_and_the_softmax_scale():
+    B, Sq, Sk, Hq, Hkv, D = 1, 9, 11, 2, 2, 8
+    q, k, v = _rand((B, Sq, Hq, D), 64), _rand((B, Sk, Hkv, D), 65), _rand((B, Sk, Hkv, D), 66)
+    o1, l1 = oracle.sdpa_fwd(q, k, v, scale=0.5, causal=True)
+    o2, l2 = oracle.sdpa_fwd(q * 4.0, k, v, scale=0.125, causal=True)
+    assert np.abs(o1 - o2).max() <= 1e-12 and np.abs(l1 - l2).max() <= 1e-12
+
+
+def test_causal_rows_past_the_keys_see_every_key():
+    # top-left alignment with Sq > Sk: rows i >= Sk - 1 see all keys, exactly as without causal masking
+    B, Sq, Sk, Hq, Hkv, D = 1, 30, 12, 2, 1, 8
+    q, k, v = _rand((B, Sq, Hq, D), 67), _rand((B, Sk, Hkv, D), 68), _rand((B, Sk, Hkv, D), 69)
+    oc, lc = oracle.sdpa_fwd(q, k, v, scale=0.3, causal=True)
+    on, ln = oracle.sdpa_fwd(q, k, v, scale=0.3, causal=False)
+    assert np.array_equal(oc[:, Sk - 1:], on[:, Sk - 1:]) and np.array_equal(lc[:, :, Sk - 1:], ln[:, :, Sk - 1:])
+    assert not np.allclose(oc[:, : Sk - 1], on[:, : Sk - 1])
