@@ -157,9 +157,25 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- timing
 
-def time_steps(step, K: int, W: int, flush=None):
+# The launch queue is primed before the timed steps: a GPU-side sleep (torch's bounded
+# clock-count spin) holds the stream while the host enqueues the first steps, so that the events
+# around a step measure the device's time for it and not the host's time to prepare its launch.
+# The sleep runs before the first event, outside every timed step.
+PRIME_US_PER_STEP = 150.0
+PRIME_MAX_US = 20000.0
+PRIME_CLOCK_HZ = 2.07e9
+
+
+def prime_queue(steps: int):
+    us = min(PRIME_MAX_US, PRIME_US_PER_STEP * max(1, steps))
+    torch.cuda._sleep(int(us * 1e-6 * PRIME_CLOCK_HZ))
+
+
+def time_steps(step, K: int, W: int, flush=None, host_us=None, prime=True):
     """W untimed steps, then K steps each bracketed by CUDA events on the launching stream
-    (an optional L2 flush runs before each step, outside the events).  Returns per-step ms."""
+    (an optional L2 flush runs before each step, outside the events; unless prime is False the
+    queue is primed first).  Returns per-step ms; host_us, if given, receives the host time of
+    each step() call in us."""
     stream = torch.cuda.current_stream()
     for _ in range(W):
         if flush:
@@ -167,14 +183,26 @@ def time_steps(step, K: int, W: int, flush=None):
         step(-1)
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    if prime:
+        prime_queue(K)
     for i in range(K):
         if flush:
             flush()
         ev[i][0].record(stream)
+        t0 = time.perf_counter()
         step(i)
+        if host_us is not None:
+            host_us.append((time.perf_counter() - t0) * 1e6)
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     return [a.elapsed_time(b) for a, b in ev]
+
+
+def step_stats(ms):
+    """Mean, median, min, max and 10th / 90th percentiles of per-step times (ms)."""
+    a = np.asarray(ms, dtype=np.float64)
+    return {"mean": float(a.mean()), "median": float(np.median(a)), "min": float(a.min()), "max": float(a.max()),
+            "p10": float(np.percentile(a, 10)), "p90": float(np.percentile(a, 90)), "n": int(a.size)}
 
 
 class Flusher:
@@ -219,7 +247,7 @@ def bench_prefill(w, K, W, dev, peaks, flusher):
     launches = 1 + (1 if w.mask else 0)
     bf16 = peaks["bf16_tflops"]
     r = {"workload": w.name, "value": tflops, "unit": "TFLOP/s", "ms_per_step": avg, "flops_per_step": flops,
-         "launches_per_step": launches}
+         "launches_per_step": launches, "step_ms": step_stats(ms)}
     if w.dtype == "e4m3":
         fp8 = bf16 * FP8_PER_BF16
         qk = 2.0 * w.D * w.B * w.Hq * visible_pairs(w.Sq, w.Sk, w.causal)
@@ -262,6 +290,7 @@ def bench_varlen(w, K, W, dev, peaks, flusher):
     bf16 = peaks["bf16_tflops"]
     return {"workload": w.name, "value": tflops, "unit": "TFLOP/s", "ms_per_step": avg, "flops_per_step": flops,
             "launches_per_step": 2, "sequences": w.B, "total_tokens": int(sum(x["lengths"])),
+            "step_ms": step_stats(ms),
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": bf16, "unit": "TFLOP/s", "frac": tflops / bf16,
                          "peak_note": "bf16 burst, of " + peaks["source"], "traffic": recorded_traffic(w.name)}}
 
@@ -293,19 +322,20 @@ def bench_int8(w, K, W, dev, peaks, flusher):
     tflops = flops / (avg * 1e-3) / 1e12
     bf16 = peaks["bf16_tflops"]
     return {"workload": w.name, "value": tflops, "unit": "TFLOP/s", "ms_per_step": avg, "flops_per_step": flops,
-            "launches_per_step": 2,
+            "launches_per_step": 2, "step_ms": step_stats(ms),
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": bf16, "unit": "TFLOP/s", "frac": tflops / bf16,
                          "peak_note": "16-bit MMA (no int8 MMA on sm_103a); bf16 burst, of " + peaks["source"],
                          "traffic": recorded_traffic(w.name)}}
 
 
-def bench_decode(w, K, W, dev, peaks, page_size: int = 64):
-    """The split-KV decode over 4 rotating input sets (each far larger than L2), then the same
-    rows in page_size-row pages scattered over a pool (the paged decode).  Returns both lines."""
+def bench_decode(w, K, W, dev, peaks, page_size: int = 64, n_sets: int = 4, paged: bool = True):
+    """The split-KV decode over n_sets rotating input sets (each far larger than L2), then, if
+    paged, the same rows in page_size-row pages scattered over a pool (the paged decode).
+    Returns (contiguous line, paged line or None)."""
     import flash_attention_forward_gb300 as fa
 
     sets = []
-    for r in range(4):  # rotating buffer sets, every one far larger than L2
+    for r in range(n_sets):  # rotating buffer sets, every one far larger than L2
         x = workloads.decode_inputs(w, rotation=r, pad_value=0.0)
         d = {n: x[n].to(dev) for n in ("q", "k", "v", "kv_len")}
         d["bytes"] = decode_bytes(w, x["kv_len"].numpy())
@@ -317,11 +347,11 @@ def bench_decode(w, K, W, dev, peaks, page_size: int = 64):
     hbm = peaks["hbm_gbs"]
 
     def line(name, ms, launches, extra=None):
-        by = [sets[i % 4]["bytes"] for i in range(K)]
+        by = [sets[i % n_sets]["bytes"] for i in range(K)]
         gbs = [b / (t * 1e-3) / 1e9 for b, t in zip(by, ms)]
         value = sum(by) / (sum(ms) * 1e-3) / 1e9
         r = {"workload": name, "value": value, "unit": "GB/s", "ms_per_step": sum(ms) / K, "bytes_per_step": sum(by) / K,
-             "launches_per_step": launches, "per_step_gbs_min": min(gbs),
+             "launches_per_step": launches, "per_step_gbs_min": min(gbs), "step_ms": step_stats(ms),
              "roofline": {"bound": "hbm", "achieved": value, "peak": hbm, "unit": "GB/s", "frac": value / hbm,
                           "peak_note": "copy bandwidth, of " + peaks["source"], "traffic": recorded_traffic(name)}}
         if extra:
@@ -329,17 +359,19 @@ def bench_decode(w, K, W, dev, peaks, page_size: int = 64):
         return r
 
     def step(i):
-        s = sets[i % 4] if i >= 0 else sets[0]
+        s = sets[i % n_sets] if i >= 0 else sets[0]
         fa.sdpa_decode(s["q"], s["k"], s["v"], s["kv_len"], scale=w.scale, out=o, lse=lse, workspace=ws)
 
     contiguous = line(w.name, time_steps(step, K, W), 2)
+    if not paged:
+        return contiguous, None
     for r, d in enumerate(sets):  # the same rows, paged: every page lands at a seeded random pool slot
         d["kp"], d["vp"], d["table"] = workloads.page_caches(d["k"], d["v"], page_size, seed=100 + r, spare_pages=64)
         del d["k"], d["v"]
     torch.cuda.empty_cache()
 
     def step_paged(i):
-        s = sets[i % 4] if i >= 0 else sets[0]
+        s = sets[i % n_sets] if i >= 0 else sets[0]
         fa.sdpa_decode_paged(s["q"], s["kp"], s["vp"], s["table"], s["kv_len"], scale=w.scale, out=o, lse=lse,
                              workspace=ws)
 
@@ -364,12 +396,50 @@ def bench_e2e_prefill(w, K, dev):
     def step(_i):
         fa.sdpa_fwd_host(hq, hk, hv, scale=w.scale, causal=w.causal, out=ho, lse=hl, workspace=ws)
 
-    ms = time_steps(step, K, 3)
+    # no queue priming here: the end-to-end time includes the host's work of every call
+    ms = time_steps(step, K, 3, prime=False)
     avg = sum(ms) / len(ms)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
     return {"value": prefill_flops(w) / (avg * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": avg,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "api": "sdpa_fwd_host (pinned host buffers)"}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "api": "sdpa_fwd_host (pinned host buffers)",
+            "link": link_floor((hq, hk, hv), (ho, hl), dev)}
+
+
+def link_floor(ups, downs, dev, reps: int = 5):
+    """The host link alone on the same pinned buffers: the upward copies, the downward copies,
+    and both at once on two streams (median of reps, CUDA events).  The last is the floor of any
+    end-to-end step that moves these bytes."""
+    dups = [torch.empty_like(t, device=dev) for t in ups]
+    ddowns = [torch.empty_like(t, device=dev) for t in downs]
+    s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    n_up = sum(t.numel() * t.element_size() for t in ups)
+    n_down = sum(t.numel() * t.element_size() for t in downs)
+
+    def timed(up: bool, down: bool) -> float:
+        ts = []
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            main = torch.cuda.current_stream()
+            a.record(main)
+            for st, go, pairs in ((s_up, up, zip(dups, ups)), (s_down, down, zip(downs, ddowns))):
+                if not go:
+                    continue
+                st.wait_event(a)
+                with torch.cuda.stream(st):
+                    for dst, src in pairs:
+                        dst.copy_(src, non_blocking=True)
+                main.wait_stream(st)
+            b.record(main)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return float(np.median(ts))
+
+    t_up, t_down, t_both = timed(True, False), timed(False, True), timed(True, True)
+    return {"h2d_ms": t_up, "h2d_gbs": n_up / (t_up * 1e-3) / 1e9, "d2h_ms": t_down,
+            "d2h_gbs": n_down / (t_down * 1e-3) / 1e9, "both_concurrent_ms": t_both,
+            "note": "plain copies of the step's bytes on two streams: the floor of an end-to-end step"}
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -527,6 +597,51 @@ def profile_run(args):
                       "device_status": status}))
 
 
+def tensor_peaks(dev, n: int = 8192, reps: int = 10, sustain_s: float = 4.0):
+    """Dense GEMM throughput of the library GEMMs on this GPU, measured like the bf16 figure the
+    roofline uses: torch.matmul bf16 and torch._scaled_mm e4m3 (per-tensor scales, bf16 out) at
+    n^3, best of reps (burst) and back to back for sustain_s (sustained), CUDA events."""
+    out = {"n": n, "method": f"best of {reps} (burst) and back to back for {sustain_s} s (sustained), CUDA events"}
+    a16 = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+    b16 = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+    one = torch.ones((), device=dev, dtype=torch.float32)
+    a8 = a16.to(torch.float8_e4m3fn)
+    b8t = b16.to(torch.float8_e4m3fn).t()  # column-major second operand
+    fns = {"bf16": lambda: torch.matmul(a16, b16),
+           "e4m3": lambda: torch._scaled_mm(a8, b8t, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)}
+    flops = 2.0 * n ** 3
+    for name, fn in fns.items():
+        try:
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            best = float("inf")
+            for _ in range(reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                torch.cuda.synchronize()
+                best = min(best, e0.elapsed_time(e1))
+            count, t_end = 0, time.perf_counter() + sustain_s
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            while time.perf_counter() < t_end:
+                for _ in range(20):
+                    fn()
+                count += 20
+                torch.cuda.synchronize()
+            e1.record()
+            torch.cuda.synchronize()
+            out[name] = {"burst_tflops": flops / (best * 1e-3) / 1e12,
+                         "sustained_tflops": flops * count / (e0.elapsed_time(e1) * 1e-3) / 1e12}
+        except Exception as exc:  # noqa: BLE001 - a library without this GEMM is reported, not fatal
+            out[name] = {"unavailable": f"{type(exc).__name__}: {exc}"[:200]}
+    if "burst_tflops" in out.get("bf16", {}) and "burst_tflops" in out.get("e4m3", {}):
+        out["e4m3_per_bf16_burst"] = out["e4m3"]["burst_tflops"] / out["bf16"]["burst_tflops"]
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -538,9 +653,21 @@ def main():
     ap.add_argument("--profile", metavar="WORKLOAD", help="only run WORKLOAD's launches (for ncu captures)")
     ap.add_argument("--batch", type=int, default=0, help="with --profile: override the batch size")
     ap.add_argument("--page-size", type=int, default=0, help="with --profile on the decode: a paged cache of this page size")
+    ap.add_argument("--tensor-peaks", action="store_true",
+                    help="only measure the dense bf16 and e4m3 library GEMM throughput (with clocks) and exit")
     args = ap.parse_args()
     if args.profile:
         profile_run(args)
+        return
+    if args.tensor_peaks:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        for n in (8192, 16384):
+            sampler = ClockSampler(dev.index or 0)
+            sampler.start()
+            res = tensor_peaks(dev, n=n)
+            res["clocks"] = sampler.stop()
+            print(json.dumps({"tensor_peaks": res}), flush=True)
+            torch.cuda.empty_cache()
         return
     args.warmup = max(args.warmup, 3)
     rank, local, world = dist_setup()
@@ -568,7 +695,8 @@ def main():
         time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
-    ms = time_steps(step, args.steps, 0, flusher)
+    host_us = []
+    ms = time_steps(step, args.steps, 0, flusher, host_us=host_us)
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop() if rank == 0 else None
@@ -599,6 +727,11 @@ def main():
         dec, dec_paged = bench_decode(workloads.WORKLOADS["splitkv_decode_bf16_d128"], k2, args.warmup, dev, peaks)
         others[dec["workload"]] = dec
         others[dec_paged["workload"]] = dec_paged
+        del dec_paged
+        torch.cuda.empty_cache()
+        mla, _ = bench_decode(workloads.WORKLOADS["mla_decode_bf16_d192_g16"], k2, args.warmup, dev, peaks, n_sets=2,
+                              paged=False)
+        others[mla["workload"]] = mla
         torch.cuda.empty_cache()
 
     cpu = None
@@ -619,7 +752,13 @@ def main():
                          "peak_note": "bf16 dense burst, of " + peaks["source"]},
             "cpu_baseline": None if cpu is None else {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")},
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
-                    "d2h_bytes_per_step": e2e["d2h_bytes_per_step"], "api": e2e["api"]},
+                    "d2h_bytes_per_step": e2e["d2h_bytes_per_step"], "api": e2e["api"], "ms_per_step": e2e_ms,
+                    "link": e2e["link"]},
+            "step_ms": step_stats(ms),
+            "host_us_per_call": {"median": float(np.median(host_us)), "max": float(np.max(host_us))},
+            "timing": "CUDA events around each step on the launching stream; the launch queue is primed by a "
+                      "GPU-side sleep before the first step (outside every event), so the events measure the "
+                      "device's time per step",
             "gpu_launches": args.steps,
             "clocks": clocks,
             "device_status": fa.sdpa_status_string(ok_status),

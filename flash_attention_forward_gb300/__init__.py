@@ -135,6 +135,41 @@ def _i64(vals):
     return arr
 
 
+def _on_device(**tensors):
+    """Every given tensor (None skipped) must be a CUDA tensor on the current device with a unit
+    innermost stride: the library takes raw device pointers for the current device's stream."""
+    dev = torch.cuda.current_device() if torch.cuda.is_available() else None
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+        if t.device.index != dev:
+            raise ValueError(f"{name} is on {t.device}, not on the current device cuda:{dev}")
+        if t.dim() > 0 and t.stride(-1) != 1:
+            raise ValueError(f"{name} must have a unit innermost stride")
+
+
+def _int32_vector(name, t, n=None):
+    if t.dtype != torch.int32 or t.dim() != 1 or (n is not None and t.numel() != n):
+        raise ValueError(f"{name} must be an int32 vector" + ("" if n is None else f" of {n} entries"))
+
+
+def _check_decode(q, k, v, kv_len, out, lse, cache_dims=4):
+    if q.dim() != 3 or k.dim() != cache_dims or v.dim() != cache_dims:
+        raise ValueError("q must be [B, Hq, D] and the caches [*, rows, Hkv, D|Dv]")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q and the caches must share one dtype")
+    _on_device(q=q, k_cache=k, v_cache=v, kv_len=kv_len, out=out, lse=lse)
+    _int32_vector("kv_len", kv_len, q.shape[0])
+    B, Hq, _ = q.shape
+    Dv = v.shape[-1]
+    if out is not None and (tuple(out.shape) != (B, Hq, Dv) or out.dtype != q.dtype):
+        raise ValueError(f"out must be a {q.dtype} tensor of shape {(B, Hq, Dv)}")
+    if lse is not None and (tuple(lse.shape) != (B, Hq) or lse.dtype != torch.float32 or not lse.is_contiguous()):
+        raise ValueError(f"lse must be a contiguous fp32 tensor of shape {(B, Hq)}")
+
+
 def sdpa_fwd_workspace_size(B: int, Hq: int, Sq: int, Sk: int, Dv: int, causal: bool, has_mask: bool) -> int:
     """Bytes of prefill workspace for the current device: the condensed mask (required with a
     mask) followed by the partials of the split last round of work tiles (optional)."""
@@ -151,9 +186,7 @@ def _fwd_args(q, k, v, out, lse, mask, workspace, out_dtype, return_lse, causal)
     B, Sq, Hq, D = q.shape
     _, Sk, Hkv, _ = k.shape
     Dv = v.shape[-1]
-    for t in (q, k, v):
-        if not t.is_cuda or t.stride(-1) != 1:
-            raise ValueError("q, k, v must be CUDA tensors with unit innermost stride")
+    _on_device(q=q, k=k, v=v, out=out, lse=lse, mask=mask, workspace=workspace)
     if out is None:
         out = torch.empty((B, Sq, Hq, Dv), dtype=out_dtype, device=q.device)
     if lse is None and return_lse:
@@ -219,12 +252,10 @@ def _varlen_args(q, k, v, cu_seqlens_q, cu_seqlens_k, out, lse, workspace, out_d
     total_q, Hq, D = q.shape
     total_k, Hkv, _ = k.shape
     Dv = v.shape[-1]
-    for t in (q, k, v):
-        if not t.is_cuda or t.stride(-1) != 1:
-            raise ValueError("q, k, v must be CUDA tensors with unit innermost stride")
+    _on_device(q=q, k=k, v=v, cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k, out=out, lse=lse,
+               workspace=workspace)
     for t, name in ((cu_seqlens_q, "cu_seqlens_q"), (cu_seqlens_k, "cu_seqlens_k")):
-        if t.dtype != torch.int32 or not t.is_cuda or t.dim() != 1 or t.stride(0) != 1:
-            raise ValueError(f"{name} must be a contiguous int32 CUDA vector")
+        _int32_vector(name, t)
     B = cu_seqlens_q.numel() - 1
     if cu_seqlens_k.numel() != B + 1:
         raise ValueError("cu_seqlens_q and cu_seqlens_k must both hold B + 1 offsets")
@@ -296,9 +327,8 @@ def sdpa_fwd_int8(q, k, v, q_scale, k_scale, v_scale=None, *, scale: float | Non
         raise ValueError("q, k, v must be [B, S, H, D]")
     B, Sq, Hq, D = q.shape
     _, Sk, Hkv, _ = k.shape
-    for t in (q, k, v):
-        if not t.is_cuda or t.stride(-1) != 1:
-            raise ValueError("q, k, v must be CUDA tensors with unit innermost stride")
+    _on_device(q=q, k=k, v=v, q_scale=q_scale, k_scale=k_scale, v_scale=v_scale, out=out, lse=lse,
+               workspace=workspace)
     nqb, nkb = (Sq + 127) // 128, (Sk + 127) // 128
     checks = [(q_scale, (B, Hq, nqb), "q_scale"), (k_scale, (B, Hkv, nkb), "k_scale")]
     if v_scale is not None:
@@ -366,13 +396,11 @@ def sdpa_fwd_host(q, k, v, *, scale: float | None = None, causal: bool = False, 
 def sdpa_decode(q, k_cache, v_cache, kv_len, *, scale: float | None = None, out=None, lse=None,
                 return_lse: bool = True, workspace=None, stream=None):
     """Decode: q [B,Hq,D], caches [B,max_kv,Hkv,D|Dv], kv_len int32 [B] (device).  Returns (o, lse)."""
-    if q.dim() != 3 or k_cache.dim() != 4 or v_cache.dim() != 4:
-        raise ValueError("q must be [B, Hq, D], caches [B, max_kv, Hkv, D]")
+    _check_decode(q, k_cache, v_cache, kv_len, out, lse)
+    _on_device(workspace=workspace)
     B, Hq, D = q.shape
     _, max_kv, Hkv, _ = k_cache.shape
     Dv = v_cache.shape[-1]
-    if kv_len.dtype != torch.int32 or not kv_len.is_cuda:
-        raise ValueError("kv_len must be an int32 CUDA tensor")
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     if out is None:
         out = torch.empty((B, Hq, Dv), dtype=q.dtype, device=q.device)
@@ -393,17 +421,14 @@ def sdpa_decode_paged(q, k_pool, v_pool, page_table, kv_len, *, scale: float | N
                       return_lse: bool = True, workspace=None, stream=None):
     """Decode over a paged cache: q [B,Hq,D], pools [n_pages,page_size,Hkv,D|Dv], page_table int32
     [B, max_pages] (device; logical page -> physical page), kv_len int32 [B] (device)."""
-    if q.dim() != 3 or k_pool.dim() != 4 or v_pool.dim() != 4 or page_table.dim() != 2:
-        raise ValueError("q must be [B, Hq, D], pools [n_pages, page_size, Hkv, D], page_table [B, max_pages]")
+    _check_decode(q, k_pool, v_pool, kv_len, out, lse)
+    _on_device(page_table=page_table, workspace=workspace)
+    if page_table.dim() != 2 or page_table.dtype != torch.int32 or page_table.shape[0] != q.shape[0]:
+        raise ValueError("page_table must be an int32 [B, max_pages] tensor")
     B, Hq, D = q.shape
     n_pages, page_size, Hkv, _ = k_pool.shape
     Dv = v_pool.shape[-1]
     max_pages = page_table.shape[1]
-    for t, name in ((kv_len, "kv_len"), (page_table, "page_table")):
-        if t.dtype != torch.int32 or not t.is_cuda:
-            raise ValueError(f"{name} must be an int32 CUDA tensor")
-    if page_table.stride(1) != 1:
-        raise ValueError("page_table rows must be contiguous")
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     if out is None:
         out = torch.empty((B, Hq, Dv), dtype=q.dtype, device=q.device)
@@ -439,6 +464,7 @@ def sdpa_decode_noalloc(q, k_cache, v_cache, kv_len, *, scale: float | None = No
     Such callers pass ``out`` (and ``lse``) themselves; this wrapper only allocates them when they
     are omitted.  The first call on a device resolves the array's address and should precede any
     stream capture; calls that overlap on the GPU share the array and race."""
+    _check_decode(q, k_cache, v_cache, kv_len, out, lse)
     lib = _load()
     fn = lib.sdpa_decode_noalloc
     p, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float

@@ -15,27 +15,28 @@ namespace {
 __device__ uint32_t g_status_word;
 }  // namespace
 
-constexpr int kMaxDevices = 64;
-uint32_t* g_status_ptr[kMaxDevices] = {};
-std::mutex g_mu;
+std::atomic<uint32_t*> g_status_ptr[kMaxDevices] = {};
+std::atomic<int> g_sm_count[kMaxDevices] = {};
 
 namespace {
 std::atomic<int> g_stall_next{0};
 
-// Device address of this device's status word (looked up once per device).
+// Device address of this device's status word (looked up once per device; a race between two
+// first calls resolves the same address twice).
 cudaError_t status_ptr(uint32_t** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_status_ptr[dev] == nullptr) {
+  uint32_t* ptr = g_status_ptr[dev].load(std::memory_order_acquire);
+  if (ptr == nullptr) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_status_word);
     if (e != cudaSuccess) return e;
-    g_status_ptr[dev] = static_cast<uint32_t*>(p);
+    ptr = static_cast<uint32_t*>(p);
+    g_status_ptr[dev].store(ptr, std::memory_order_release);
   }
-  *out = g_status_ptr[dev];
+  *out = ptr;
   return cudaSuccess;
 }
 
@@ -60,6 +61,19 @@ EncodeTiledFn encode_fn() {
 }  // namespace
 
 cudaError_t device_status_ptr(uint32_t** out) { return status_ptr(out); }
+
+cudaError_t current_device_sms(int* dev, int* sms) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return e;
+  if (*dev < 0 || *dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  int n = g_sm_count[*dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if ((e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, *dev)) != cudaSuccess) return e;
+    g_sm_count[*dev].store(n, std::memory_order_relaxed);
+  }
+  *sms = n;
+  return cudaSuccess;
+}
 
 bool encode_bshd(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int esize, int B, int S, int H, int Dh,
                  int64_t sb, int64_t ss, int64_t sh, int box0, int box_rows, CUtensorMapSwizzle sw) {
@@ -92,7 +106,7 @@ size_t mask_ws_bytes(int B, int Sq, int Sk) {
 // Split plan of a prefill launch on the current device (no split if the device query fails).
 SplitPlan fwd_split_plan(int B, int Hq, int Sq, int Sk, bool causal) {
   int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+  if (current_device_sms(&dev, &sms) != cudaSuccess) {
     cudaGetLastError();  // clear the error so that later calls do not see it
     return SplitPlan{};
   }
@@ -298,6 +312,87 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
 }
 
 }  // namespace
+
+size_t decode_partials_bytes(int B, int Hq, int max_kv, int Dv) {
+  const size_t n_splits = (size_t)((max_kv + kDecodeSplit - 1) / kDecodeSplit);
+  return round16((size_t)B * Hq * n_splits * (size_t)(Dv + 2) * sizeof(float));
+}
+
+int decode_check(const void* q, const void* k, const void* v, const int32_t* page_table, const int32_t* kv_len,
+                 void* o, float* lse, int B, int Hq, int Hkv, int max_kv, int page_size, int max_pages, int n_pages,
+                 int D, int Dv, const int64_t* strides, float scale, int dtype, DecodeCall* call) {
+  const bool paged = page_table != nullptr;
+  if (!q || !k || !v || !kv_len || !o) return SDPA_ERR_INVALID;
+  if (B < 1 || Hq < 1 || Hkv < 1 || max_kv < 1 || D < 1 || Dv < 1) return SDPA_ERR_INVALID;
+  if (Hq % Hkv != 0) return SDPA_ERR_INVALID;
+  if (!(std::isfinite(scale) && scale > 0.f)) return SDPA_ERR_INVALID;
+  if (paged && (page_size & (page_size - 1))) return SDPA_ERR_INVALID;  // a power of two
+  if (dtype != SDPA_F16 && dtype != SDPA_BF16) return SDPA_ERR_UNSUPPORTED;
+  // head dims: (128, 128) and the MLA shape (192, 128)
+  if (!((D == 128 || D == 192) && Dv == kDecodeDv)) return SDPA_ERR_UNSUPPORTED;
+  if (paged && page_size < 16) return SDPA_ERR_UNSUPPORTED;
+  const int group = Hq / Hkv;
+  if (group > 16) return SDPA_ERR_UNSUPPORTED;  // one 16-row tensor-core tile per KV head
+  if (B > 65535 || Hkv > 65535) return SDPA_ERR_UNSUPPORTED;
+  // element strides {q_b, q_h, k_b, k_s, k_h, v_b, v_s, v_h, o_b, o_h} (+ page-table row stride)
+  int64_t st[SDPA_DECODE_PAGED_NSTRIDES];
+  const int rows = paged ? page_size : max_kv;  // rows of one batch entry of the caches
+  if (strides) {
+    std::memcpy(st, strides, sizeof(int64_t) * (paged ? SDPA_DECODE_PAGED_NSTRIDES : SDPA_DECODE_NSTRIDES));
+  } else {
+    const int64_t cs[SDPA_DECODE_PAGED_NSTRIDES] = {(int64_t)Hq * D,  D,  (int64_t)rows * Hkv * D, (int64_t)Hkv * D,
+                                                    D, (int64_t)rows * Hkv * Dv, (int64_t)Hkv * Dv, Dv,
+                                                    (int64_t)Hq * Dv, Dv, max_pages};
+    std::memcpy(st, cs, sizeof(st));
+  }
+  for (int i = 0; i < SDPA_DECODE_NSTRIDES; ++i)
+    if (!stride_ok(st[i], 8)) return SDPA_ERR_UNSUPPORTED;  // 16-byte rows for TMA and vector loads
+  if (paged && st[10] < max_pages) return SDPA_ERR_INVALID;  // page-table rows hold max_pages entries
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return SDPA_ERR_UNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(kv_len) & 3u) return SDPA_ERR_INVALID;
+  if (paged && (reinterpret_cast<uintptr_t>(page_table) & 3u)) return SDPA_ERR_INVALID;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SDPA_ERR_INVALID;
+
+  DecodeParams& p = call->p;
+  p = DecodeParams{};
+  p.q = q, p.k = k, p.v = v, p.kv_len = kv_len, p.o = o, p.lse = lse;
+  p.q_b = st[0], p.q_h = st[1], p.k_b = st[2], p.k_s = st[3], p.k_h = st[4];
+  p.v_b = st[5], p.v_s = st[6], p.v_h = st[7], p.o_b = st[8], p.o_h = st[9];
+  p.B = B, p.Hq = Hq, p.Hkv = Hkv, p.max_kv = max_kv, p.group = group;
+  p.n_splits_max = (max_kv + kDecodeSplit - 1) / kDecodeSplit;
+  p.scale2 = (float)((double)scale * 1.4426950408889634);
+  if (paged) {
+    p.page_table = page_table;
+    p.pt_b = st[10];
+    p.page_size = page_size;
+    p.log2_page = __builtin_ctz((unsigned)page_size);
+    p.max_pages = max_pages;
+    p.n_pages = n_pages;
+  }
+  call->elem = dtype == SDPA_BF16 ? kBF16 : kF16;
+  call->D = D, call->Dv = Dv;
+  call->map_b = paged ? n_pages : B;
+  call->map_s = rows;
+  call->box_rows = paged && page_size < 64 ? page_size : 64;  // a box never spans two pages
+  return SDPA_OK;
+}
+
+int decode_launch(DecodeCall& call, float* ws, cudaStream_t st) {
+  DecodeParams& p = call.p;
+  const CUtensorMapDataType dt = call.elem == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  alignas(64) CUtensorMap tk, tv;
+  if (!encode_bshd(&tk, p.k, dt, 2, call.map_b, call.map_s, p.Hkv, call.D, p.k_b, p.k_s, p.k_h, 64, call.box_rows,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_bshd(&tv, p.v, dt, 2, call.map_b, call.map_s, p.Hkv, call.Dv, p.v_b, p.v_s, p.v_h, 64, call.box_rows,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+    return SDPA_ERR_CUDA;
+  uint32_t* status = nullptr;
+  if (status_ptr(&status) != cudaSuccess) return SDPA_ERR_CUDA;
+  p.ws = ws;
+  p.status = status;
+  return launch_decode(call.elem, call.D, p, tk, tv, st) == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
 }  // namespace sdpa
 
 using namespace sdpa;
@@ -589,129 +684,37 @@ int sdpa_fwd_host(const void* q, const void* k, const void* v, void* o, float* l
 
 size_t sdpa_decode_workspace_size(int B, int Hq, int max_kv, int Dv) {
   if (B < 1 || Hq < 1 || max_kv < 1 || Dv < 1) return 0;
-  const size_t n_splits = (size_t)((max_kv + kDecodeSplit - 1) / kDecodeSplit);
-  return round16((size_t)B * Hq * n_splits * (size_t)(Dv + 2) * sizeof(float));
+  return decode_partials_bytes(B, Hq, max_kv, Dv);
 }
 
 int sdpa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_len, void* o, float* lse,
                 int B, int Hq, int Hkv, int max_kv, int D, int Dv, const int64_t* strides, float scale,
                 void* workspace, size_t workspace_bytes, sdpa_dtype dtype, void* stream) {
-  if (!q || !k_cache || !v_cache || !kv_len || !o) return SDPA_ERR_INVALID;
-  if (B < 1 || Hq < 1 || Hkv < 1 || max_kv < 1 || D < 1 || Dv < 1) return SDPA_ERR_INVALID;
-  if (Hq % Hkv != 0) return SDPA_ERR_INVALID;
-  if (!(std::isfinite(scale) && scale > 0.f)) return SDPA_ERR_INVALID;
-  if (dtype != SDPA_F16 && dtype != SDPA_BF16) return SDPA_ERR_UNSUPPORTED;
-  if (D != 128 || Dv != kDecodeDv) return SDPA_ERR_UNSUPPORTED;
-  const int group = Hq / Hkv;
-  if (group > 8) return SDPA_ERR_UNSUPPORTED;
-  if (B > 65535 || Hkv > 65535) return SDPA_ERR_UNSUPPORTED;
-  int64_t st[SDPA_DECODE_NSTRIDES];
-  if (strides) {
-    std::memcpy(st, strides, sizeof(st));
-  } else {
-    const int64_t cs[SDPA_DECODE_NSTRIDES] = {(int64_t)Hq * D, D, (int64_t)max_kv * Hkv * D, (int64_t)Hkv * D, D,
-                                              (int64_t)max_kv * Hkv * Dv, (int64_t)Hkv * Dv, Dv, (int64_t)Hq * Dv,
-                                              Dv};
-    std::memcpy(st, cs, sizeof(st));
-  }
-  for (int i = 0; i < SDPA_DECODE_NSTRIDES; ++i)
-    if (!stride_ok(st[i], 8)) return SDPA_ERR_UNSUPPORTED;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o)) return SDPA_ERR_UNSUPPORTED;
-  if (reinterpret_cast<uintptr_t>(kv_len) & 3u) return SDPA_ERR_INVALID;
-  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SDPA_ERR_INVALID;
-  if (!workspace || !aligned16(workspace) || workspace_bytes < sdpa_decode_workspace_size(B, Hq, max_kv, Dv))
+  DecodeCall call;
+  const int rc = decode_check(q, k_cache, v_cache, nullptr, kv_len, o, lse, B, Hq, Hkv, max_kv, 0, 0, 0, D, Dv,
+                              strides, scale, dtype, &call);
+  if (rc != SDPA_OK) return rc;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < decode_partials_bytes(B, Hq, max_kv, Dv))
     return SDPA_ERR_INVALID;
-
-  const CUtensorMapDataType dt = dtype == SDPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  alignas(64) CUtensorMap tk, tv;
-  if (!encode_bshd(&tk, k_cache, dt, 2, B, max_kv, Hkv, D, st[2], st[3], st[4], 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_bshd(&tv, v_cache, dt, 2, B, max_kv, Hkv, Dv, st[5], st[6], st[7], 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
-    return SDPA_ERR_CUDA;
-  uint32_t* status = nullptr;
-  if (status_ptr(&status) != cudaSuccess) return SDPA_ERR_CUDA;
-
-  DecodeParams p{};
-  p.q = q, p.k = k_cache, p.v = v_cache, p.kv_len = kv_len, p.o = o, p.lse = lse;
-  p.ws = static_cast<float*>(workspace);
-  p.status = status;
-  p.q_b = st[0], p.q_h = st[1], p.k_b = st[2], p.k_s = st[3], p.k_h = st[4];
-  p.v_b = st[5], p.v_s = st[6], p.v_h = st[7], p.o_b = st[8], p.o_h = st[9];
-  p.B = B, p.Hq = Hq, p.Hkv = Hkv, p.max_kv = max_kv, p.group = group;
-  p.n_splits_max = (max_kv + kDecodeSplit - 1) / kDecodeSplit;
-  p.scale2 = (float)((double)scale * 1.4426950408889634);
-  const cudaError_t e =
-      launch_decode(dtype == SDPA_BF16 ? kBF16 : kF16, p, tk, tv, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+  return decode_launch(call, static_cast<float*>(workspace), static_cast<cudaStream_t>(stream));
 }
 
 int sdpa_decode_paged(const void* q, const void* k_pool, const void* v_pool, const int32_t* page_table,
                       const int32_t* kv_len, void* o, float* lse, int B, int Hq, int Hkv, int page_size, int max_pages,
                       int n_pages, int D, int Dv, const int64_t* strides, float scale, void* workspace,
                       size_t workspace_bytes, sdpa_dtype dtype, void* stream) {
-  if (!q || !k_pool || !v_pool || !page_table || !kv_len || !o) return SDPA_ERR_INVALID;
-  if (B < 1 || Hq < 1 || Hkv < 1 || page_size < 1 || max_pages < 1 || n_pages < 1 || D < 1 || Dv < 1)
-    return SDPA_ERR_INVALID;
-  if (Hq % Hkv != 0) return SDPA_ERR_INVALID;
-  if (!(std::isfinite(scale) && scale > 0.f)) return SDPA_ERR_INVALID;
-  if (page_size & (page_size - 1)) return SDPA_ERR_INVALID;  // a power of two
-  if (dtype != SDPA_F16 && dtype != SDPA_BF16) return SDPA_ERR_UNSUPPORTED;
-  if (D != 128 || Dv != kDecodeDv) return SDPA_ERR_UNSUPPORTED;
-  if (page_size < 16) return SDPA_ERR_UNSUPPORTED;
-  const int group = Hq / Hkv;
-  if (group > 8) return SDPA_ERR_UNSUPPORTED;
-  if (B > 65535 || Hkv > 65535) return SDPA_ERR_UNSUPPORTED;
+  if (!page_table) return SDPA_ERR_INVALID;
+  if (page_size < 1 || max_pages < 1 || n_pages < 1) return SDPA_ERR_INVALID;
   const long long max_kv_ll = (long long)max_pages * page_size;
   if (max_kv_ll > (1ll << 30)) return SDPA_ERR_UNSUPPORTED;
   const int max_kv = (int)max_kv_ll;
-  int64_t st[SDPA_DECODE_PAGED_NSTRIDES];
-  if (strides) {
-    std::memcpy(st, strides, sizeof(st));
-  } else {
-    const int64_t cs[SDPA_DECODE_PAGED_NSTRIDES] = {(int64_t)Hq * D, D, (int64_t)page_size * Hkv * D, (int64_t)Hkv * D, D,
-                                                    (int64_t)page_size * Hkv * Dv, (int64_t)Hkv * Dv, Dv,
-                                                    (int64_t)Hq * Dv, Dv, max_pages};
-    std::memcpy(st, cs, sizeof(st));
-  }
-  for (int i = 0; i < SDPA_DECODE_NSTRIDES; ++i)
-    if (!stride_ok(st[i], 8)) return SDPA_ERR_UNSUPPORTED;
-  if (st[10] < max_pages) return SDPA_ERR_INVALID;  // page-table rows hold max_pages entries
-  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(o)) return SDPA_ERR_UNSUPPORTED;
-  if ((reinterpret_cast<uintptr_t>(kv_len) & 3u) || (reinterpret_cast<uintptr_t>(page_table) & 3u))
+  DecodeCall call;
+  const int rc = decode_check(q, k_pool, v_pool, page_table, kv_len, o, lse, B, Hq, Hkv, max_kv, page_size,
+                              max_pages, n_pages, D, Dv, strides, scale, dtype, &call);
+  if (rc != SDPA_OK) return rc;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < decode_partials_bytes(B, Hq, max_kv, Dv))
     return SDPA_ERR_INVALID;
-  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SDPA_ERR_INVALID;
-  if (!workspace || !aligned16(workspace) || workspace_bytes < sdpa_decode_workspace_size(B, Hq, max_kv, Dv))
-    return SDPA_ERR_INVALID;
-
-  // the pools as [n_pages, page_size, Hkv, .] tensors: a box is min(64, page_size) rows of one page
-  const CUtensorMapDataType dt = dtype == SDPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  const int box_rows = page_size < 64 ? page_size : 64;
-  alignas(64) CUtensorMap tk, tv;
-  if (!encode_bshd(&tk, k_pool, dt, 2, n_pages, page_size, Hkv, D, st[2], st[3], st[4], 64, box_rows,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_bshd(&tv, v_pool, dt, 2, n_pages, page_size, Hkv, Dv, st[5], st[6], st[7], 64, box_rows,
-                   CU_TENSOR_MAP_SWIZZLE_128B))
-    return SDPA_ERR_CUDA;
-  uint32_t* status = nullptr;
-  if (status_ptr(&status) != cudaSuccess) return SDPA_ERR_CUDA;
-
-  DecodeParams p{};
-  p.q = q, p.k = k_pool, p.v = v_pool, p.kv_len = kv_len, p.o = o, p.lse = lse;
-  p.ws = static_cast<float*>(workspace);
-  p.status = status;
-  p.q_b = st[0], p.q_h = st[1], p.k_b = st[2], p.k_s = st[3], p.k_h = st[4];
-  p.v_b = st[5], p.v_s = st[6], p.v_h = st[7], p.o_b = st[8], p.o_h = st[9];
-  p.B = B, p.Hq = Hq, p.Hkv = Hkv, p.max_kv = max_kv, p.group = group;
-  p.n_splits_max = (max_kv + kDecodeSplit - 1) / kDecodeSplit;
-  p.scale2 = (float)((double)scale * 1.4426950408889634);
-  p.page_table = page_table;
-  p.pt_b = st[10];
-  p.page_size = page_size;
-  p.log2_page = __builtin_ctz((unsigned)page_size);
-  p.max_pages = max_pages;
-  p.n_pages = n_pages;
-  const cudaError_t e =
-      launch_decode(dtype == SDPA_BF16 ? kBF16 : kF16, p, tk, tv, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+  return decode_launch(call, static_cast<float*>(workspace), static_cast<cudaStream_t>(stream));
 }
 
 int sdpa_check_device_status(void* stream) {

@@ -26,21 +26,23 @@ namespace {
 constexpr float kDecodeRescaleLog2 = 8.0f;
 constexpr float kLn2f = 0.6931471805599453f;
 
+// D (16 x 8, fp32) += A (16 x 16) B (16 x 8): A rows 0-7 are query heads g of the GQA group
+// (a0, a2), rows 8-15 heads g + 8 (a1, a3; zero for groups of at most 8 heads).
 template <int ELEM>
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
-  // rows 8..15 of A (a1, a3) are zero: only the first 8 rows carry query heads
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
   if constexpr (ELEM == kBF16) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
         "{%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
   } else {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
         "{%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
   }
 }
 
@@ -77,16 +79,17 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 }
 
 // Phase 1 layout.  A CTA is 4 consumer warps plus one producer warp.  The producer streams the
-// split's keys in chunks of kDecChunk rows: two 64-column TMA boxes of K and two of V per chunk
-// (128-byte swizzle) into a kDecStages-deep shared-memory ring.  Consumer warp w takes rows
-// [16 w, 16 w + 16) of every chunk, copies its fragments to registers and releases the stage at
-// once.
+// split's keys in chunks of kDecChunk rows: D / 64 64-column TMA boxes of K and two of V per
+// chunk (128-byte swizzle) into a DecCfg<D, WIDE>::STAGES-deep shared-memory ring.  Consumer warp w
+// takes rows [16 w, 16 w + 16) of every chunk, copies its fragments to registers and releases
+// the stage.
 //
-// Fragments (m16n8k16): g = lane / 4 is the query head of the group for A/C rows and the key
-// (QK) or value column (PV) for B; t = lane % 4.
+// Fragments (m16n8k16): g = lane / 4 is the query head of the group for A/C rows (rows 0-7:
+// heads g; rows 8-15: heads g + 8, used by groups of 9-16 heads) and the key (QK) or value
+// column (PV) for B; t = lane % 4.
 //  * Head dimension, permuted consistently for Q and K: thread t owns dims [32 i + 8 t, +8)
-//    for i = 0..3; k-step kk uses chunk i = kk / 2, words 2 (kk%2) and 2 (kk%2) + 1.  A dot
-//    product does not depend on the order of its terms.
+//    for i = 0 .. D/32 - 1; k-step kk uses chunk i = kk / 2, words 2 (kk%2) and 2 (kk%2) + 1.
+//    A dot product does not depend on the order of its terms.
 //  * Keys: QK n-index n of n-tile nt is key 8 nt + kSigma[n] of the warp's 16, and P.V k-index
 //    k is the same key as QK's (nt, n) = (k / 8, k % 8).  Any fixed order of keys gives the
 //    same softmax; this one spreads the eight rows a quarter-warp reads over all swizzle phases.
@@ -94,11 +97,21 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 //    operand for all 16 n-tiles is one 32-byte run of a value row; the C fragment of thread
 //    (g, t) ends up holding value dims 16 kBeta[2t] + nt and 16 kBeta[2t + 1] + nt.
 constexpr int kDecChunk = 64;                           // keys per TMA chunk
-constexpr int kDecStages = 3;
 constexpr int kDecBox = kDecChunk * 64 * 2;             // one 64-column box of 16-bit rows: 8 KB
-constexpr int kDecStageBytes = 4 * kDecBox;             // K (2 boxes) + V (2 boxes)
-constexpr int kDecSmem = kDecStages * kDecStageBytes + 256 + 1024;
 constexpr int kDecThreads = (kDecodeWarps + 1) * 32;
+// The D = 128 kernel for groups of up to 8 heads fits two CTAs per SM (at most ~200 registers a
+// thread) with a 3-stage ring each; the wider variants (groups of 9-16 heads, or D = 192) need
+// more registers, run one CTA per SM and keep about as many bytes in flight with a deeper ring.
+template <int D, bool WIDE>
+struct DecCfg {
+  static constexpr int KBOX = D / 64;                       // K boxes per chunk (V: 2, Dv = 128)
+  static constexpr int QCH = D / 32;                        // 8-dim runs of the head dim per thread
+  static constexpr int STAGE = (KBOX + 2) * kDecBox;        // 32 KB (D = 128) or 40 KB (D = 192)
+  static constexpr bool TWO_CTAS = D == 128 && !WIDE;
+  static constexpr int STAGES = TWO_CTAS ? 3 : (D == 128 ? 6 : 5);
+  static constexpr int SMEM = STAGES * STAGE + 256 + 1024;
+  static_assert(D % 64 == 0 && STAGES * STAGE >= kDecodeWarps * 16 * kDecodeDv * 4, "merge buffer fits the ring");
+};
 __constant__ int kSigma[8] = {0, 4, 1, 5, 2, 6, 3, 7};
 __constant__ int kBeta[8] = {0, 2, 1, 3, 4, 6, 5, 7};
 
@@ -109,15 +122,20 @@ __device__ __forceinline__ uint32_t swz(int row, int unit) {
 
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
 
-template <int ELEM, bool PAGED>
+// WIDE: groups of 9-16 query heads per KV head (rows 8-15 of the tiles carry heads 8-15).
+template <int ELEM, bool PAGED, int D, bool WIDE>
 __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
-                                                                   const __grid_constant__ CUtensorMap tm_v,
-                                                                   const DecodeParams p) {
+                                                                      const __grid_constant__ CUtensorMap tm_v,
+                                                                      const DecodeParams p) {
+  using C = DecCfg<D, WIDE>;
+  constexpr int ST = C::STAGES;
+  constexpr int RH = WIDE ? 2 : 1;  // row halves of the tiles that carry heads
+  constexpr int R = 8 * RH;         // heads per warp in the merge buffer
   extern __shared__ uint8_t dsmem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kDecStages * kDecStageBytes);
-  uint64_t* empty = full + kDecStages;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kDecStages);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + ST * C::STAGE);
+  uint64_t* empty = full + ST;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + ST);
 
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -128,7 +146,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const __grid_
   const int nchunks = (end - start + kDecChunk - 1) / kDecChunk;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kDecStages; ++s) {
+    for (int s = 0; s < ST; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kDecodeWarps);
     }
@@ -137,31 +155,32 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const __grid_
   }
   __syncthreads();
 
-  __shared__ float sm_m[kDecodeWarps][8];
-  __shared__ float sm_l[kDecodeWarps][8];
+  __shared__ float sm_m[kDecodeWarps][R];
+  __shared__ float sm_l[kDecodeWarps][R];
   const int G = p.group;
 
   if (warp == kDecodeWarps) {
     // ---------------------------------------------------------- producer (one warp)
-    // A chunk is 4 boxes (the two 64-column halves of K and of V) for contiguous caches and pages
-    // of at least 64 rows: lane 0 issues them.  Pages of fewer rows need 4 x 64 / page_size boxes
-    // per chunk, one page each: lane 0 posts the byte count and the boxes are issued by separate
-    // lanes, so that their page-table reads and issues overlap.
+    // A chunk is KBOX + 2 boxes (the 64-column parts of K and of V) for contiguous caches and
+    // pages of at least 64 rows: lane 0 issues them.  Pages of fewer rows need (KBOX + 2) x 64 /
+    // page_size boxes per chunk, one page each: lane 0 posts the byte count and the boxes are
+    // issued by separate lanes, so that their page-table reads and issues overlap.
+    constexpr int PARTS = C::KBOX + 2;
     const int rows = PAGED ? min(kDecChunk, p.page_size) : kDecChunk;  // rows per box
-    const int nsub = kDecChunk / rows;                                 // boxes per operand half
+    const int nsub = kDecChunk / rows;                                 // boxes per operand part
     if (lane == 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
     }
     int c = 0;
     for (; c < nchunks; ++c) {
-      const int s = c % kDecStages, r = c / kDecStages;
-      uint8_t* st = smem + s * kDecStageBytes;
+      const int s = c % ST, r = c / ST;
+      uint8_t* st = smem + s * C::STAGE;
       const int row = start + c * kDecChunk;  // rows past max_kv read as zeros
       if (nsub == 1) {
         if (lane == 0) {
           if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, abort_flag, p.status)) break;
-          mbar_arrive_expect_tx(&full[s], kDecStageBytes);
+          mbar_arrive_expect_tx(&full[s], C::STAGE);
           int c3 = b, c2 = row;
           if constexpr (PAGED) {
             const int lp = row >> p.log2_page;
@@ -169,43 +188,49 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const __grid_
             c3 = lp < p.max_pages ? __ldg(p.page_table + b * p.pt_b + lp) : p.n_pages;
             c2 = row & (p.page_size - 1);
           }
-          tma_load_4d(st, &tm_k, &full[s], 0, kvh, c2, c3);
-          tma_load_4d(st + kDecBox, &tm_k, &full[s], 64, kvh, c2, c3);
-          tma_load_4d(st + 2 * kDecBox, &tm_v, &full[s], 0, kvh, c2, c3);
-          tma_load_4d(st + 3 * kDecBox, &tm_v, &full[s], 64, kvh, c2, c3);
+#pragma unroll
+          for (int kb = 0; kb < C::KBOX; ++kb) tma_load_4d(st + kb * kDecBox, &tm_k, &full[s], 64 * kb, kvh, c2, c3);
+          tma_load_4d(st + C::KBOX * kDecBox, &tm_v, &full[s], 0, kvh, c2, c3);
+          tma_load_4d(st + (C::KBOX + 1) * kDecBox, &tm_v, &full[s], 64, kvh, c2, c3);
         }
       } else {
         if (r > 0 && !mbar_wait_warp(&empty[s], (r - 1) & 1, abort_flag, p.status)) break;
-        if (lane == 0) mbar_arrive_expect_tx(&full[s], kDecStageBytes);
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], C::STAGE);
         __syncwarp();
-        if (lane < 4 * nsub) {
-          const int part = lane & 3, sub = lane >> 2;  // part: K cols 0-63, K 64-127, V 0-63, V 64-127
+        if (lane < PARTS * nsub) {
+          // part: the 64-column parts of K (KBOX of them), then V columns 0-63 and 64-127
+          const int part = lane % PARTS, sub = lane / PARTS;
           const int key = row + sub * rows;
           const int lp = key >> p.log2_page;
           const int phys = lp < p.max_pages ? __ldg(p.page_table + b * p.pt_b + lp) : p.n_pages;
+          const bool is_k = part < C::KBOX;
           // page_size is a power of two >= 16, so every box starts 2 KB-aligned in the stage
-          tma_load_4d(st + part * kDecBox + sub * rows * 128, part < 2 ? &tm_k : &tm_v, &full[s], (part & 1) * 64,
-                      kvh, 0, phys);
+          tma_load_4d(st + part * kDecBox + sub * rows * 128, is_k ? &tm_k : &tm_v, &full[s],
+                      64 * (is_k ? part : part - C::KBOX), kvh, 0, phys);
         }
       }
     }
     if (c < nchunks && lane == 0)  // aborted: let the copies in flight land
-      for (int j = max(0, c - kDecStages); j < c; ++j) mbar_drain(&full[j % kDecStages], (j / kDecStages) & 1);
+      for (int j = max(0, c - ST); j < c; ++j) mbar_drain(&full[j % ST], (j / ST) & 1);
   } else {
     // ---------------------------------------------------------- consumers
     const int g = lane >> 2, t = lane & 3;
     const float scale2 = p.scale2;
-    uint32_t qf[4][4];
-    if (g < G) {
-      const uint16_t* qrow = reinterpret_cast<const uint16_t*>(p.q) + b * p.q_b + (int64_t)(kvh * G + g) * p.q_h;
+    uint32_t qf[RH][C::QCH][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 v = ldg128(qrow + 32 * i + 8 * t);
-        qf[i][0] = v.x, qf[i][1] = v.y, qf[i][2] = v.z, qf[i][3] = v.w;
+    for (int rh = 0; rh < RH; ++rh) {
+      const int head = g + 8 * rh;
+      if (head < G) {
+        const uint16_t* qrow = reinterpret_cast<const uint16_t*>(p.q) + b * p.q_b + (int64_t)(kvh * G + head) * p.q_h;
+#pragma unroll
+        for (int i = 0; i < C::QCH; ++i) {
+          const uint4 v = ldg128(qrow + 32 * i + 8 * t);
+          qf[rh][i][0] = v.x, qf[rh][i][1] = v.y, qf[rh][i][2] = v.z, qf[rh][i][3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < C::QCH; ++i) qf[rh][i][0] = qf[rh][i][1] = qf[rh][i][2] = qf[rh][i][3] = 0u;
       }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) qf[i][0] = qf[i][1] = qf[i][2] = qf[i][3] = 0u;
     }
     const int beta_g = kBeta[g];
     int sig_k[2], sig_v[4];  // chunk rows of this thread's K (per n-tile) and V (per u) keys
@@ -214,26 +239,31 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const __grid_
 #pragma unroll
     for (int u = 0; u < 4; ++u) sig_v[u] = 16 * warp + 8 * (u >> 1) + kSigma[2 * t + (u & 1)];
 
+    // acc[nt][0..1]: heads g, acc[nt][2..3]: heads g + 8 (zero products unless WIDE)
     float acc[16][4];
 #pragma unroll
     for (int nt = 0; nt < 16; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-    float m = -INFINITY, l = 0.f;
+    float m[RH], l[RH];
+#pragma unroll
+    for (int rh = 0; rh < RH; ++rh) m[rh] = -INFINITY, l[rh] = 0.f;
     bool ok = true;
 
     for (int c = 0; c < nchunks; ++c) {
-      const int s = c % kDecStages;
-      if (!mbar_wait_warp(&full[s], (c / kDecStages) & 1, abort_flag, p.status)) {
+      const int s = c % ST;
+      if (!mbar_wait_warp(&full[s], (c / ST) & 1, abort_flag, p.status)) {
         ok = false;
         break;
       }
-      const uint8_t* kS = smem + s * kDecStageBytes;
-      const uint8_t* vS = kS + 2 * kDecBox;
+      const uint8_t* kS = smem + s * C::STAGE;
+      const uint8_t* vS = kS + C::KBOX * kDecBox;
       const int row0 = start + c * kDecChunk;  // key index of chunk row 0
-      uint4 kr[2][4];
+      // every fragment of the chunk goes to registers first, so that the stage refills while the
+      // tensor cores and the softmax work on them
+      uint4 kr[2][C::QCH];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) kr[nt][i] = lds128(kS + (i >> 1) * kDecBox + swz(sig_k[nt], (i & 1) * 4 + t));
+        for (int i = 0; i < C::QCH; ++i) kr[nt][i] = lds128(kS + (i >> 1) * kDecBox + swz(sig_k[nt], (i & 1) * 4 + t));
       uint4 vr[4][2];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -253,30 +283,51 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const __grid_
       for (int nt = 0; nt < 2; ++nt) {
         sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {
           const int i = kk >> 1, hs = kk & 1;
-          mma16816<ELEM>(sc[nt], qf[i][2 * hs], qf[i][2 * hs + 1], word(kr[nt][i], 2 * hs), word(kr[nt][i], 2 * hs + 1));
+          mma16816<ELEM>(sc[nt], qf[0][i][2 * hs], WIDE ? qf[RH - 1][i][2 * hs] : 0u, qf[0][i][2 * hs + 1],
+                         WIDE ? qf[RH - 1][i][2 * hs + 1] : 0u, word(kr[nt][i], 2 * hs), word(kr[nt][i], 2 * hs + 1));
         }
       }
-      float x[4] = {sc[0][0] * scale2, sc[0][1] * scale2, sc[1][0] * scale2, sc[1][1] * scale2};
+
+      // x[rh][u]: score of head g + 8 rh with key u ((nt, n) = (u / 2, 2t + u % 2), V row u)
+      float x[RH][4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (row0 + sig_v[u] >= end) x[u] = -INFINITY;  // (nt, n) = (u / 2, 2t + u % 2): same key as V row u
-      float mb = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
-      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
-      const float m_cand = fmaxf(m, mb);
-      if (__any_sync(0xffffffffu, m_cand > m + kDecodeRescaleLog2)) {
-        const float alpha = (m_cand == -INFINITY) ? 1.f : ex2(m - m_cand);
-        l *= alpha;
+      for (int rh = 0; rh < RH; ++rh) {
+        x[rh][0] = sc[0][2 * rh] * scale2, x[rh][1] = sc[0][2 * rh + 1] * scale2;
+        x[rh][2] = sc[1][2 * rh] * scale2, x[rh][3] = sc[1][2 * rh + 1] * scale2;
 #pragma unroll
-        for (int nt = 0; nt < 16; ++nt) acc[nt][0] *= alpha, acc[nt][1] *= alpha;
-        m = m_cand;
+        for (int u = 0; u < 4; ++u)
+          if (row0 + sig_v[u] >= end) x[rh][u] = -INFINITY;
       }
-      const float neg_m = (m == -INFINITY) ? 0.f : -m;
-      const uint32_t a0 = pack2<ELEM>(ex2(x[0] + neg_m), ex2(x[1] + neg_m));
-      const uint32_t a2 = pack2<ELEM>(ex2(x[2] + neg_m), ex2(x[3] + neg_m));
-      l += sum2<ELEM>(a0) + sum2<ELEM>(a2);
+      float m_cand[RH];
+      bool need = false;
+#pragma unroll
+      for (int rh = 0; rh < RH; ++rh) {
+        float mb = fmaxf(fmaxf(x[rh][0], x[rh][1]), fmaxf(x[rh][2], x[rh][3]));
+        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+        m_cand[rh] = fmaxf(m[rh], mb);
+        need |= m_cand[rh] > m[rh] + kDecodeRescaleLog2;
+      }
+      if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int rh = 0; rh < RH; ++rh) {
+          const float alpha = (m_cand[rh] == -INFINITY) ? 1.f : ex2(m[rh] - m_cand[rh]);
+          l[rh] *= alpha;
+#pragma unroll
+          for (int nt = 0; nt < 16; ++nt) acc[nt][2 * rh] *= alpha, acc[nt][2 * rh + 1] *= alpha;
+          m[rh] = m_cand[rh];
+        }
+      }
+      uint32_t a[RH][2];  // P as the A operand: keys (2t, 2t + 1) and (2t + 8, 2t + 9) of each head row
+#pragma unroll
+      for (int rh = 0; rh < RH; ++rh) {
+        const float neg_m = (m[rh] == -INFINITY) ? 0.f : -m[rh];
+        a[rh][0] = pack2<ELEM>(ex2(x[rh][0] + neg_m), ex2(x[rh][1] + neg_m));
+        a[rh][1] = pack2<ELEM>(ex2(x[rh][2] + neg_m), ex2(x[rh][3] + neg_m));
+        l[rh] += sum2<ELEM>(a[rh][0]) + sum2<ELEM>(a[rh][1]);
+      }
       // O += P V over the 16 keys, 16 n-tiles of 8 (permuted) value columns
 #pragma unroll
       for (int nt = 0; nt < 16; ++nt) {
@@ -284,29 +335,36 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const __grid_
         const uint32_t sel = (nt & 1) ? 0x7632u : 0x5410u;
         const uint32_t b0 = prmt(word(vr[0][hv], wi), word(vr[1][hv], wi), sel);
         const uint32_t b1 = prmt(word(vr[2][hv], wi), word(vr[3][hv], wi), sel);
-        mma16816<ELEM>(acc[nt], a0, a2, b0, b1);
+        mma16816<ELEM>(acc[nt], a[0][0], WIDE ? a[RH - 1][0] : 0u, a[0][1], WIDE ? a[RH - 1][1] : 0u, b0, b1);
       }
     }
 
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
-    if (!ok) {
-      m = -INFINITY;
-      l = 0.f;
+#pragma unroll
+    for (int rh = 0; rh < RH; ++rh) {
+      l[rh] += __shfl_xor_sync(0xffffffffu, l[rh], 1);
+      l[rh] += __shfl_xor_sync(0xffffffffu, l[rh], 2);
+      if (!ok) {
+        m[rh] = -INFINITY;
+        l[rh] = 0.f;
+      }
     }
     // merge the four warps: per-warp O goes to the (now idle) ring memory
     __syncwarp();
     asm volatile("bar.sync 1, %0;" ::"n"(kDecodeWarps * 32));  // all consumers are past the ring
-    float* sm_o = reinterpret_cast<float*>(smem);               // [warp][row][dv]
-    if (g < G) {
+    float* sm_o = reinterpret_cast<float*>(smem);               // [warp][head][dv]
 #pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        sm_o[(warp * 8 + g) * kDecodeDv + 16 * kBeta[2 * t] + nt] = acc[nt][0];
-        sm_o[(warp * 8 + g) * kDecodeDv + 16 * kBeta[2 * t + 1] + nt] = acc[nt][1];
-      }
-      if (t == 0) {
-        sm_m[warp][g] = m;
-        sm_l[warp][g] = l;
+    for (int rh = 0; rh < RH; ++rh) {
+      const int head = g + 8 * rh;
+      if (head < G) {
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+          sm_o[(warp * R + head) * kDecodeDv + 16 * kBeta[2 * t] + nt] = acc[nt][2 * rh];
+          sm_o[(warp * R + head) * kDecodeDv + 16 * kBeta[2 * t + 1] + nt] = acc[nt][2 * rh + 1];
+        }
+        if (t == 0) {
+          sm_m[warp][head] = m[rh];
+          sm_l[warp][head] = l[rh];
+        }
       }
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kDecodeWarps * 32));
@@ -321,7 +379,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const __grid_
       for (int wi = 0; wi < kDecodeWarps; ++wi) {
         const float mw = sm_m[wi][r];
         const float e = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-        o += e * sm_o[(wi * 8 + r) * kDecodeDv + dv];
+        o += e * sm_o[(wi * R + r) * kDecodeDv + dv];
         ls += e * sm_l[wi][r];
       }
       const int h = kvh * G + r;
@@ -482,30 +540,42 @@ __global__ void __launch_bounds__(1024) varlen_prep_kernel(const VarlenPrepParam
   }
 }
 
-template <int ELEM, bool PAGED>
+template <int ELEM, bool PAGED, int D, bool WIDE>
+cudaError_t launch_split_instance(dim3 grid, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
+                                  cudaStream_t st) {
+  int dev = 0, sms = 0;
+  cudaError_t e = current_device_sms(&dev, &sms);
+  if (e != cudaSuccess) return e;
+  static std::atomic<uint64_t> opted{0};
+  auto kern = decode_split_kernel<ELEM, PAGED, D, WIDE>;
+  if ((e = smem_opt_in(kern, DecCfg<D, WIDE>::SMEM, dev, opted)) != cudaSuccess) return e;
+  kern<<<grid, kDecThreads, DecCfg<D, WIDE>::SMEM, st>>>(tk, tv, p);
+  return cudaGetLastError();
+}
+
+template <int ELEM, int D>
 cudaError_t launch_split(dim3 grid, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                          cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<ELEM, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kDecSmem);
-  if (e != cudaSuccess) return e;
-  decode_split_kernel<ELEM, PAGED><<<grid, kDecThreads, kDecSmem, st>>>(tk, tv, p);
-  return cudaGetLastError();
+  const bool wide = p.group > 8;
+  if (p.page_table)
+    return wide ? launch_split_instance<ELEM, true, D, true>(grid, tk, tv, p, st)
+                : launch_split_instance<ELEM, true, D, false>(grid, tk, tv, p, st);
+  return wide ? launch_split_instance<ELEM, false, D, true>(grid, tk, tv, p, st)
+              : launch_split_instance<ELEM, false, D, false>(grid, tk, tv, p, st);
 }
 
 }  // namespace
 
-cudaError_t launch_decode(int elem, const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+cudaError_t launch_decode(int elem, int D, const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                           cudaStream_t st) {
   const dim3 g1(p.n_splits_max, p.Hkv, p.B), g2(p.Hq, p.B);
   cudaError_t e;
   if (elem == kBF16) {
-    if (p.page_table) e = launch_split<kBF16, true>(g1, tk, tv, p, st);
-    else e = launch_split<kBF16, false>(g1, tk, tv, p, st);
+    e = D == 192 ? launch_split<kBF16, 192>(g1, tk, tv, p, st) : launch_split<kBF16, 128>(g1, tk, tv, p, st);
     if (e != cudaSuccess) return e;
     decode_combine_kernel<kBF16><<<g2, kDecodeDv, 0, st>>>(p);
   } else {
-    if (p.page_table) e = launch_split<kF16, true>(g1, tk, tv, p, st);
-    else e = launch_split<kF16, false>(g1, tk, tv, p, st);
+    e = D == 192 ? launch_split<kF16, 192>(g1, tk, tv, p, st) : launch_split<kF16, 128>(g1, tk, tv, p, st);
     if (e != cudaSuccess) return e;
     decode_combine_kernel<kF16><<<g2, kDecodeDv, 0, st>>>(p);
   }

@@ -2,6 +2,7 @@
 // C-ABI layer.  Internal: not part of the public header.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
@@ -172,11 +173,48 @@ cudaError_t launch_prefill_bf16_block_scaled(int D, bool causal, const CUtensorM
 cudaError_t launch_prefill_e4m3(int D, int Dv, bool causal, bool has_mask, const CUtensorMap& tq,
                                 const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st,
                                 bool* supported);
-cudaError_t launch_decode(int elem, const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+
+cudaError_t launch_decode(int elem, int D, const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                           cudaStream_t st);
+
+// The decode entry points share one validated call description, built without any CUDA call,
+// and one launch path; they differ only in where the per-split partials go.
+struct DecodeCall {
+  DecodeParams p;          // every field but ws and status
+  int elem, D, Dv;
+  int map_b, map_s;        // tensor-map extents: [map_b, map_s, Hkv, .] (batch x max_kv, or pages x page_size)
+  int box_rows;            // rows of one TMA box
+};
+// Validates a decode call (page_table null: contiguous caches [B, max_kv, Hkv, .], else pools
+// [n_pages, page_size, Hkv, .] with max_kv = max_pages * page_size) and fills *call.  Returns 0
+// or the public status code (invalid / unsupported) of the first argument that fails.
+int decode_check(const void* q, const void* k, const void* v, const int32_t* page_table, const int32_t* kv_len,
+                 void* o, float* lse, int B, int Hq, int Hkv, int max_kv, int page_size, int max_pages, int n_pages,
+                 int D, int Dv, const int64_t* strides, float scale, int dtype, DecodeCall* call);
+// Bytes of per-split partial results of a decode: [B, Hq, n_splits, Dv + 2] fp32, 16-byte rounded.
+size_t decode_partials_bytes(int B, int Hq, int max_kv, int Dv);
+// Encodes the tensor maps and launches both phases with the partials in ws; 0 or the public
+// status code of a CUDA failure.
+int decode_launch(DecodeCall& call, float* ws, cudaStream_t st);
 
 // Device address of the current device's status word.
 cudaError_t device_status_ptr(uint32_t** out);
+
+// The current device and its SM count; the count is looked up on the first call per device and
+// kept, so a launch costs no device query.
+constexpr int kMaxDevices = 64;
+cudaError_t current_device_sms(int* dev, int* sms);
+
+// One-time opt-in of kernel `kern` to `bytes` of dynamic shared memory on device `dev`; `done`
+// (one per kernel) records the devices already set up, one bit each.
+template <typename Kernel>
+cudaError_t smem_opt_in(Kernel kern, int bytes, int dev, std::atomic<uint64_t>& done) {
+  const uint64_t bit = uint64_t(1) << (dev & 63);
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 // Tensor map of a [B, S, H, Dh] tensor (element strides sb, ss, sh; innermost stride 1) with a
 // box of box0 x 1 x box_rows x 1 elements; false if the driver rejects it.

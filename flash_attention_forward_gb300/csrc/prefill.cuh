@@ -36,7 +36,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 template <int ELEM, int D, int DV>
 struct PrefillCfg {
-  static constexpr int ESZ = (ELEM == kE4M3) ? 1 : 2;
+  static constexpr int ESZ = (ELEM == kE4M3) ? 1 : 2;  // Q and K element bytes
   static constexpr int CH = 64;                 // elements per swizzle chunk (TMA box width)
   static constexpr int CHB = CH * ESZ;          // 128 B (16-bit) or 64 B (e4m3)
   static constexpr uint32_t SW = (CHB == 128) ? kSwizzle128B : kSwizzle64B;
@@ -79,6 +79,7 @@ template <>
 struct ElemTraits<kE4M3> {
   static constexpr uint32_t qk_fmt = 0, pv_fmt = 0;  // e4m3 x e4m3 (kind::f8f6f4), P and V f16
 };
+
 
 template <int ELEM>
 __device__ __forceinline__ uint32_t pack_p(float lo, float hi) {
@@ -447,6 +448,69 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         // Ring block of step j: e4m3 uses block g + j for K(j) and g + j - 1 for V(j-1); the
         // 16-bit ring holds both operands of step j in one stage.
         for (int j = 0; ok && j <= w.n_blocks; ++j) {
+          // Steady steps 2 <= j < min(n_t) - 1: both tiles take P.V of block j - 1 (neither the
+          // first nor the last of the tile) and QK of block j (not the last), so no o_empty wait,
+          // o_full or q_empty commit is due.  The same waits and commits as the general step
+          // below, in the same order, without its per-step case analysis: every instruction the
+          // issuing thread spends between MMA groups can leave the tensor pipe idle.
+          if (j == 2) {
+            const int j_end = min(w.n_t[0], w.n_t[1]) - 1;
+            for (; j < j_end; ++j) {
+              const int gk = (ELEM == kE4M3) ? g + j : g;      // stage of K(j)
+              const int gv = (ELEM == kE4M3) ? g + j - 1 : g;  // stage of V(j-1)
+              const int s = gk % ST, sv = gv % ST;
+              bool k_ready = ELEM != kE4M3 || T0_COVERS_STEP;
+              if constexpr (!T0_COVERS_STEP) {
+                if (!mbar_wait(ELEM == kE4M3 ? &v_ready[sv] : &in_full[s], ((ELEM == kE4M3 ? gv : gk) / ST) & 1,
+                               abort_flag, p.status)) {
+                  ok = false;
+                  break;
+                }
+              }
+              tc_fence_after();
+              const uint32_t dv = v_lo + static_cast<uint32_t>((sv * C::V_BYTES) >> 4);
+              const uint32_t dk = k_lo + static_cast<uint32_t>((s * C::K_BYTES) >> 4);
+#pragma unroll
+              for (int t = 0; t < kTilesPerCta; ++t) {
+                const uint32_t tS = tmem_base + t * 128;
+                const uint32_t tO = tmem_base + 256 + t * 128;
+                if (!mbar_wait(&p_full[t], pn[t] & 1, abort_flag, p.status)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < C::PV_STEPS; ++kk)
+                  mma_f16_ts(tO, tS + kk * 8, dv + static_cast<uint32_t>((kk * 16 * 128) >> 4), v_hi, idesc_pv, 1u);
+                ++pn[t];
+                if (ELEM == kE4M3 && t == kTilesPerCta - 1) mma_commit(&v_free[sv]);
+                if (!k_ready) {
+                  if (!mbar_wait(&in_full[s], (gk / ST) & 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                  }
+                  tc_fence_after();
+                  k_ready = true;
+                }
+                const uint32_t dq = q_lo + static_cast<uint32_t>((t * C::Q_BYTES) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < C::QK_STEPS; ++kk) {
+                  constexpr int kCh = kBlockQ * C::CHB;
+                  const uint32_t off = static_cast<uint32_t>(
+                      ((kk / C::STEPS_PER_CH) * kCh + (kk % C::STEPS_PER_CH) * C::KSTEP_BYTES) >> 4);
+                  if constexpr (ELEM == kE4M3)
+                    mma_f8_ss(tS, dq + off, q_hi, dk + off, k_hi, idesc_qk, kk > 0 ? 1u : 0u);
+                  else
+                    mma_f16_ss(tS, dq + off, q_hi, dk + off, k_hi, idesc_qk, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&s_full[t]);
+              }
+              if (!ok) break;
+              mma_commit(&released[s]);
+              if (ELEM != kE4M3) ++g;
+            }
+            if (!ok) break;
+          }
           const int gk = (ELEM == kE4M3) ? g + j : g;            // stage of K(j)
           const int gv = (ELEM == kE4M3) ? g + j - 1 : g;        // stage of V(j-1)
           const int s = gk % ST, r = gk / ST;

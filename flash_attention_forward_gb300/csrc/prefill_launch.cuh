@@ -10,13 +10,13 @@ cudaError_t launch_prefill_instance(const CUtensorMap& tq, const CUtensorMap& tk
                                     const PrefillParams& p, cudaStream_t st) {
   using C = PrefillCfg<ELEM, D, DV>;
   auto kern = prefill_kernel<ELEM, D, DV, CAUSAL, MASK, VAR>;
-  // the shared-memory opt-in is per device; setting it again is harmless
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  if (e != cudaSuccess) return e;
   // persistent: one CTA per SM (shared memory admits no second one), looping over work units
   int dev = 0, sms = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  cudaError_t e = current_device_sms(&dev, &sms);
+  if (e != cudaSuccess) return e;
+  // the shared-memory opt-in is per device and made once
+  static std::atomic<uint64_t> opted{0};
+  if ((e = smem_opt_in(kern, C::SMEM, dev, opted)) != cudaSuccess) return e;
   const long long units = p.n_units;
   const unsigned grid = (unsigned)(units < sms ? units : sms);
   // Group KV units so that a group is a whole number of snake round pairs (2 x grid work

@@ -78,8 +78,7 @@ __global__ void __launch_bounds__(256) widen_kernel(const WidenParams p) {
 cudaError_t launch_widen(const WidenParams& p, cudaStream_t st) {
   int dev = 0, sms = 0;
   cudaError_t e;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if ((e = current_device_sms(&dev, &sms)) != cudaSuccess) return e;
   long long groups = 0;
   for (int i = 0; i < p.n_seg; ++i)
     groups = max(groups, static_cast<long long>(p.seg[i].B) * p.seg[i].S * p.seg[i].H * (p.seg[i].Dh / 16));

@@ -30,6 +30,11 @@ def test_host_tensors_are_refused():
                                 kv_len=[3, 64])
     with pytest.raises(ValueError):
         fa.sdpa_decode(d["q"], d["k"], d["v"], d["kv_len"])
+    with pytest.raises(ValueError):
+        fa.sdpa_decode_noalloc(d["q"], d["k"], d["v"], d["kv_len"])
+    kp, vp, table = workloads.page_caches(d["k"], d["v"], 16, seed=3)
+    with pytest.raises(ValueError):
+        fa.sdpa_decode_paged(d["q"], kp, vp, table, d["kv_len"])
 
 
 def test_missing_library_fails_loudly():

@@ -94,7 +94,8 @@ def test_fp8_and_decode_validation_codes(lib):
     assert dec(wsb=100) == fa.SDPA_ERR_INVALID
     assert dec(Hkv=3) == fa.SDPA_ERR_INVALID
     assert dec(D=64, Dv=64) == fa.SDPA_ERR_UNSUPPORTED
-    assert dec(Hq=32, Hkv=2) == fa.SDPA_ERR_UNSUPPORTED  # group of 16
+    assert dec(D=192, Dv=192) == fa.SDPA_ERR_UNSUPPORTED  # value dim 128 only
+    assert dec(Hq=34, Hkv=2) == fa.SDPA_ERR_UNSUPPORTED  # group of 17: more than one 16-row tile
     assert dec(dt=fa.SDPA_E4M3) == fa.SDPA_ERR_UNSUPPORTED
     assert dec(max_kv=0) == fa.SDPA_ERR_INVALID
 

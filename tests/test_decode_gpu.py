@@ -23,12 +23,15 @@ def _run(x, dtype_scale, **kw):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
-@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (8, 8), (16, 2), (8, 1)])
-def test_ragged_lengths_nan_padding(dtype, Hq, Hkv):
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (8, 8), (16, 2), (8, 1), (12, 1), (16, 1), (32, 2)])
+@pytest.mark.parametrize("D", [128, 192])
+def test_ragged_lengths_nan_padding(dtype, Hq, Hkv, D):
     # lengths around the 16-key step, the 256-key warp share and the 1024-key split, and 0;
-    # padding rows are NaN, so reading any of them would poison the output
+    # padding rows are NaN, so reading any of them would poison the output.  Groups of 9-16
+    # query heads use the second half of the tensor-core tile's rows; D = 192 with Dv = 128 is
+    # the MLA-shaped head of the "MlaMmaOp" page.
     lens = [0, 1, 15, 16, 17, 255, 256, 257, 1023, 1024, 1025, 2047, 2048, 2049, 3000, 4096]
-    w = W.with_shape(B=len(lens), Hq=Hq, Hkv=Hkv, Sk=4096, dtype=dtype)
+    w = W.with_shape(B=len(lens), Hq=Hq, Hkv=Hkv, Sk=4096, dtype=dtype, D=D)
     x = workloads.decode_inputs(w, kv_len=lens)
     o, lse = _run(x, w.scale)
     ref_o, ref_lse = oracle.sdpa_decode(x["q"], x["k"], x["v"], x["kv_len"], scale=w.scale)
@@ -48,9 +51,10 @@ def test_decode_workload_sampled_sequences():
     assert torch.isfinite(o).all() and torch.isfinite(lse).all()
 
 
-def test_decode_equals_prefill_with_one_query():
+@pytest.mark.parametrize("D", [128, 192])
+def test_decode_equals_prefill_with_one_query(D):
     # the split/combine result equals the unsplit prefill kernel on the same keys (Sq = 1)
-    w = W.with_shape(B=2, Sk=5000)
+    w = W.with_shape(B=2, Sk=5000, D=D)
     x = workloads.decode_inputs(w, kv_len=[5000, 3333], pad_value=0.0)
     o, _ = _run(x, w.scale)
     for b, L in enumerate([5000, 3333]):
@@ -93,10 +97,10 @@ def _paged(x, page_size, spare=5, garbage=True, seed=11):
 
 
 @pytest.mark.parametrize("page_size", [16, 32, 64, 128, 256])
-@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (8, 1)])
-def test_paged_decode_matches_oracle(page_size, Hq, Hkv):
+@pytest.mark.parametrize("Hq,Hkv,D", [(32, 8, 128), (8, 1, 128), (16, 1, 128), (16, 1, 192)])
+def test_paged_decode_matches_oracle(page_size, Hq, Hkv, D):
     lens = [0, 1, 15, 16, 63, 64, 65, 1023, 1024, 1025, 3000]
-    w = W.with_shape(B=len(lens), Hq=Hq, Hkv=Hkv, Sk=4096)
+    w = W.with_shape(B=len(lens), Hq=Hq, Hkv=Hkv, Sk=4096, D=D)
     x = workloads.decode_inputs(w, kv_len=lens)
     kp, vp, table = _paged(x, page_size)
     o, lse = fa.sdpa_decode_paged(x["q"].to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV), x["kv_len"].to(DEV),

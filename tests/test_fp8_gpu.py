@@ -69,3 +69,20 @@ def test_mla_fp8_workload_sampled_rows():
     assert_close(got_o, ref_o, TOL_FP8)
     assert_lse_close(got_lse, ref_lse, TOL_LSE_F16)
     assert torch.isfinite(o).all()
+
+
+def test_strided_v():
+    # a V whose rows are strided (a slice of a wider tensor): its raw e4m3 boxes come in by TMA with
+    # the caller's row stride
+    B, Hq, Hkv, Sq, Sk, D, Dv = 1, 2, 2, 200, 333, 128, 128
+    x = workloads.custom_prefill(B, Hq, Hkv, Sq, Sk, D, Dv, dtype="e4m3", seed=77)
+    wide = torch.zeros((B, Sk, Hkv, 2 * Dv), dtype=torch.uint8, device=DEV)
+    wide[..., :Dv] = x["v"].view(torch.uint8).to(DEV)
+    v = wide.view(torch.float8_e4m3fn)[..., :Dv]
+    sq, sk, sv = x["descale"]
+    o, lse = fa.sdpa_fwd_fp8(x["q"].to(DEV), x["k"].to(DEV), v, sq, sk, sv, scale=1 / np.sqrt(D), causal=True)
+    torch.cuda.synchronize()
+    assert fa.sdpa_check_device_status() == fa.SDPA_OK
+    ref_o, ref_lse = oracle.sdpa_fwd(x["q"], x["k"], x["v"], scale=1 / np.sqrt(D), causal=True, descale=x["descale"])
+    assert_close(o.float().cpu().numpy(), ref_o, TOL_FP8)
+    assert_lse_close(lse.cpu().numpy(), ref_lse, TOL_LSE_F16)

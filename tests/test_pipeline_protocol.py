@@ -9,7 +9,8 @@ no role can move is a deadlock.  The protocol as built (tile 0's softmax waits f
 j+1 before it signals P_0(j), so the MMA thread skips that wait) must show neither, for rings
 of 2 and 4 stages and work tiles whose second query tile is empty, equal, or one block longer.
 A variant in which tile 1's softmax would take its S from the step's `released` commit, which
-the MMA thread never waits on in work tiles without tile 1, must be caught.
+the MMA thread never waits on in work tiles without tile 1, must be caught.  The protocol with
+P signalled in two halves (p_half, then p_full) is checked the same way.
 """
 import random
 
@@ -24,7 +25,7 @@ class _Bar:
         self.phase += 1
 
 
-def _run(units, stages, seed, tile1_on_released=False):
+def _run(units, stages, seed, tile1_on_released=False, p_half=False):
     rnd = random.Random(seed)
     bars = {}
 
@@ -68,6 +69,8 @@ def _run(units, stages, seed, tile1_on_released=False):
                     if j >= 1 and j - 1 < nt[t]:
                         if j == 1 and qn[t] > 0:
                             yield ("wait", bar(f"o_empty{t}"), qn[t] - 1)
+                        if p_half:  # the first half of P, for the first half of the P.V MMAs
+                            yield ("wait", bar(f"p_half{t}"), pn[t])
                         yield ("wait", bar(f"p_full{t}"), pn[t])
                         pn[t] += 1
                         if j == nt[t]:
@@ -97,6 +100,8 @@ def _run(units, stages, seed, tile1_on_released=False):
                     yield ("wait", bar(f"released{G % stages}"), G // stages)
                 else:
                     yield ("wait", bar(f"s_full{t}"), sn)
+                if p_half:
+                    yield ("do", bar(f"p_half{t}"))
                 if t == 0:
                     G = g0 + j + 1
                     yield ("wait", bar(f"in_full{G % stages}"), G // stages)
@@ -152,11 +157,14 @@ def _random_units(rnd):
     return units
 
 
+@pytest.mark.parametrize("p_half", [False, True])
 @pytest.mark.parametrize("stages", [2, 4])
-def test_protocol_has_no_alias_or_deadlock(stages):
+def test_protocol_has_no_alias_or_deadlock(stages, p_half):
+    # p_half: the softmax also signals the first half of P (keys 0-63) before the second, and the
+    # MMA thread issues the first half of the P.V MMAs on it
     for seed in range(1500):
         units = _random_units(random.Random(seed))
-        assert _run(units, stages, seed) is None, units
+        assert _run(units, stages, seed, p_half=p_half) is None, units
 
 
 def test_model_catches_a_tile_waiting_on_a_barrier_nobody_waits_for():
@@ -164,7 +172,7 @@ def test_model_catches_a_tile_waiting_on_a_barrier_nobody_waits_for():
     assert sum(f is not None for f in failures) > 50
 
 
-def _run_e4m3(units, stages, seed, t0_covers=True):
+def _run_e4m3(units, stages, seed, t0_covers=True, p_half=False):
     """The e4m3 ring: K(j) and raw V(j) load one step ahead of P.V(j); two converter warps turn
     raw V into f16 (v_ready), free the raw buffer themselves (vraw_free) and write the converted
     buffer only after the P.V that last read it (v_free).  With t0_covers, tile 0's softmax waits
@@ -230,6 +238,8 @@ def _run_e4m3(units, stages, seed, t0_covers=True):
                     if j >= 1 and j - 1 < nt[t]:
                         if j == 1 and qn[t] > 0:
                             yield ("wait", bar(f"o_empty{t}"), qn[t] - 1)
+                        if p_half:  # the first half of P, for the first half of the P.V MMAs
+                            yield ("wait", bar(f"p_half{t}"), pn[t])
                         yield ("wait", bar(f"p_full{t}"), pn[t])
                         pn[t] += 1
                         if j == nt[t]:
@@ -260,6 +270,8 @@ def _run_e4m3(units, stages, seed, t0_covers=True):
                 continue
             for j in range(nt[t]):
                 yield ("wait", bar(f"s_full{t}"), sn)
+                if p_half:
+                    yield ("do", bar(f"p_half{t}"))
                 if t == 0 and t0_covers:
                     G = g0 + j
                     yield ("wait", bar(f"v_ready{G % stages}"), G // stages)
@@ -303,9 +315,10 @@ def _run_e4m3(units, stages, seed, t0_covers=True):
     return None
 
 
+@pytest.mark.parametrize("p_half", [False, True])
 @pytest.mark.parametrize("t0_covers", [False, True])
 @pytest.mark.parametrize("stages", [2, 4])
-def test_e4m3_protocol_has_no_alias_or_deadlock(stages, t0_covers):
+def test_e4m3_protocol_has_no_alias_or_deadlock(stages, t0_covers, p_half):
     for seed in range(1000):
         units = _random_units(random.Random(seed))
-        assert _run_e4m3(units, stages, seed, t0_covers=t0_covers) is None, units
+        assert _run_e4m3(units, stages, seed, t0_covers=t0_covers, p_half=p_half) is None, units

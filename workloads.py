@@ -75,6 +75,10 @@ WORKLOADS = {
         # int8 Q/K codes with per-128-row-block scales, fp16 V (the SageV1 instance's head dim 128)
         Workload("int8_qk_causal_prefill_d128", 7, "prefill", B=2, Hq=32, Hkv=8, Sq=4096, Sk=4096, D=128,
                  Dv=128, dtype="i8", dist="normal", causal=True, out_dtype="f16", extra={"v": "f16"}),
+        # MLA-shaped decode (QK over 192 dims, 128 value dims, as in the "MlaMmaOp" prefill) with 16
+        # query heads per KV head, the widest group one decode tile holds
+        Workload("mla_decode_bf16_d192_g16", 8, "decode", B=64, Hq=64, Hkv=4, Sq=1, Sk=16384, D=192, Dv=128,
+                 dtype="bf16", dist="normal", out_dtype="bf16", kv_len_range=(1024, 16384)),
         # packed sequences: B sequence lengths drawn uniformly from len_range, keys = queries
         Workload("varlen_causal_prefill_bf16_d128", 6, "varlen", B=16, Hq=32, Hkv=8, Sq=8192, Sk=8192, D=128,
                  Dv=128, dtype="bf16", dist="normal", causal=True, out_dtype="bf16",
