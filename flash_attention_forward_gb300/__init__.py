@@ -459,7 +459,8 @@ def sdpa_check_device_status(stream=None) -> int:
 def sdpa_decode_noalloc(q, k_cache, v_cache, kv_len, *, scale: float | None = None, out=None, lse=None,
                         return_lse: bool = True, stream=None):
     """sdpa_decode without a workspace: the per-split partials go to a fixed 32 MiB array inside
-    the library, for callers that cannot allocate device memory (e.g. under CUDA graph capture).
+    the library, for callers that cannot allocate device memory (an allocator-free runtime, a host
+    that hands out device memory only through its own pool, a hot path that must not call cudaMalloc).
 
     Such callers pass ``out`` (and ``lse``) themselves; this wrapper only allocates them when they
     are omitted.  The first call on a device resolves the array's address and should precede any

@@ -1,8 +1,9 @@
 // sdpa_decode_noalloc: the split-KV decode for callers that cannot allocate device memory.
 //
-// Some callers cannot call cudaMalloc at the point where they run attention: code that runs
-// while a CUDA graph is being captured, allocator-free embedded runtimes, and hosts that hand
-// out device memory only through their own pool and forbid library allocations.  sdpa_decode
+// Some callers cannot call cudaMalloc at the point where they run attention: allocator-free
+// embedded runtimes, hosts that hand out device memory only through their own pool and forbid
+// library allocations, and serving loops that must not call cudaMalloc on the hot path (it can
+// synchronize the device).  sdpa_decode
 // already allocates nothing, but it needs a caller-provided workspace for the per-split
 // partial results.  This entry point takes that workspace from a fixed array in the
 // library's own device memory instead, so the caller passes only inputs and outputs.

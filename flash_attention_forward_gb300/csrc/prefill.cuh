@@ -261,7 +261,8 @@ __device__ __forceinline__ int nth_item(int k) {
 //   v_free[s]               : P V(j) finished (converted buffer free)
 //   v_ready[s]              : V(j) converted to f16
 //   s_full[t]               : S_t = Q_t K^T finished
-//   p_full[t]               : P_t written to tensor memory (and O_t rescaled if needed)
+//   p_half[t]               : keys 0-63 of P_t written to tensor memory (and O_t rescaled if needed)
+//   p_full[t]               : all of P_t written
 //   o_full[t]               : the last P_t V of the work tile finished (epilogue may read O_t)
 // A rescale of O_t needs no barrier of its own: the commit behind s_full[t] for block j also
 // covers the P_t V of block j-1, which the same thread issued earlier.
@@ -298,7 +299,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   uint64_t* o_full = p_full + 2;           // [2]
   uint64_t* o_empty = o_full + 2;          // [2]
   uint64_t* mma_done = o_empty + 2;        // [1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* p_half = mma_done + 1;         // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(p_half + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x;
@@ -314,6 +316,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       mbar_init(&q_empty[t], 1);
       mbar_init(&s_full[t], 1);
       mbar_init(&p_full[t], 128);
+      mbar_init(&p_half[t], 128);
       mbar_init(&o_full[t], 1);
       mbar_init(&o_empty[t], 128);
     }
@@ -474,14 +477,19 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
               for (int t = 0; t < kTilesPerCta; ++t) {
                 const uint32_t tS = tmem_base + t * 128;
                 const uint32_t tO = tmem_base + 256 + t * 128;
-                if (!mbar_wait(&p_full[t], pn[t] & 1, abort_flag, p.status)) {
-                  ok = false;
-                  break;
-                }
-                tc_fence_after();
+                // P.V in two halves: keys 0-63 as soon as the softmax has written them
 #pragma unroll
-                for (int kk = 0; kk < C::PV_STEPS; ++kk)
-                  mma_f16_ts(tO, tS + kk * 8, dv + static_cast<uint32_t>((kk * 16 * 128) >> 4), v_hi, idesc_pv, 1u);
+                for (int h = 0; h < 2; ++h) {
+                  if (!mbar_wait(h == 0 ? &p_half[t] : &p_full[t], pn[t] & 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                  }
+                  tc_fence_after();
+#pragma unroll
+                  for (int kk = h * C::PV_STEPS / 2; kk < (h + 1) * C::PV_STEPS / 2; ++kk)
+                    mma_f16_ts(tO, tS + kk * 8, dv + static_cast<uint32_t>((kk * 16 * 128) >> 4), v_hi, idesc_pv, 1u);
+                }
+                if (!ok) break;
                 ++pn[t];
                 if (ELEM == kE4M3 && t == kTilesPerCta - 1) mma_commit(&v_free[sv]);
                 if (!k_ready) {
@@ -542,16 +550,22 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                 ok = false;
                 break;
               }
-              if (!mbar_wait(&p_full[t], pn[t] & 1, abort_flag, p.status)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
               const uint32_t dv = v_lo + static_cast<uint32_t>((sv * C::V_BYTES) >> 4);
               const uint32_t acc0 = (j - 1 > 0) ? 1u : 0u;
+              // P.V in two halves: keys 0-63 as soon as the softmax has written them
 #pragma unroll
-              for (int kk = 0; kk < C::PV_STEPS; ++kk)
-                mma_f16_ts(tO, tS + kk * 8, dv + static_cast<uint32_t>((kk * 16 * 128) >> 4), v_hi, idesc_pv, kk > 0 ? 1u : acc0);
+              for (int h = 0; h < 2; ++h) {
+                if (!mbar_wait(h == 0 ? &p_half[t] : &p_full[t], pn[t] & 1, abort_flag, p.status)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = h * C::PV_STEPS / 2; kk < (h + 1) * C::PV_STEPS / 2; ++kk)
+                  mma_f16_ts(tO, tS + kk * 8, dv + static_cast<uint32_t>((kk * 16 * 128) >> 4), v_hi, idesc_pv,
+                             kk > 0 ? 1u : acc0);
+              }
+              if (!ok) break;
               if (j == w.n_t[t]) mma_commit(&o_full[t]);  // O_t of this work tile complete
               ++pn[t];
             }
@@ -760,66 +774,74 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           l *= alpha;
           m_used = m_cand;
         }
-        // P = exp2(blk_scale2 * s - m), rounded to 16 bits; l sums the rounded values
+        // P = exp2(blk_scale2 * s - m), rounded to 16 bits; l sums the rounded values.  P goes to
+        // tensor memory in two halves of 64 keys, each signalled as soon as it is written
+        // (p_half, then p_full), so that the MMA thread starts P.V on the first half while the
+        // second is computed.
         const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
-        {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
           uint32_t pk[32];
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-#pragma unroll
-            for (int w2 = 0; w2 < 32; ++w2) {
-              const int c = half * 64 + 2 * w2;
-              float x0, x1;
-              ffma2_scalar(x0, x1, s[c], s[c + 1], blk_scale2, neg_m);
-              pk[w2] = pack_p<ELEM>(ex2(x0), ex2(x1));
-              if (w2 & 1)
-                acc_p_pair<ELEM>(ls[2], ls[3], pk[w2]);
-              else
-                acc_p_pair<ELEM>(ls[0], ls[1], pk[w2]);
-            }
-            tmem_st32(tS + half * 32, pk);
+          for (int w2 = 0; w2 < 32; ++w2) {
+            const int c = half * 64 + 2 * w2;
+            float x0, x1;
+            ffma2_scalar(x0, x1, s[c], s[c + 1], blk_scale2, neg_m);
+            pk[w2] = pack_p<ELEM>(ex2(x0), ex2(x1));
+            if (w2 & 1)
+              acc_p_pair<ELEM>(ls[2], ls[3], pk[w2]);
+            else
+              acc_p_pair<ELEM>(ls[0], ls[1], pk[w2]);
           }
-        }
-        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-        if (rescale && j > 0) {
-          // O holds P.V of blocks < j at the old max (finished: s_full(j) covers it); scale it
+          tmem_st32(tS + half * 32, pk);
+          if (half == 1) break;
+          if (rescale && j > 0) {
+            // O holds P.V of blocks < j at the old max (finished: s_full(j) covers it); scale it
+            // before the first P.V of block j
 #pragma unroll 1
-          for (int c = 0; c < DV / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + c * 32, o);
-            tmem_ld_wait();
-            reg_fence(o);
+            for (int c = 0; c < DV / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(tO + c * 32, o);
+              tmem_ld_wait();
+              reg_fence(o);
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              float a = __uint_as_float(o[i]), b = __uint_as_float(o[i + 1]);
-              fmul2_scalar(a, b, alpha);
-              o[i] = __float_as_uint(a);
-              o[i + 1] = __float_as_uint(b);
-            }
-            tmem_st32(tO + c * 32, o);
-          }
-        }
-        // P_0(j) also stands for what the MMA thread's step j+1 reads, so it skips its own waits
-        // at that step.  Tile 0 is active in every work tile, and the MMA thread waits for itself
-        // at every step tile 0 does not cover, so these waits never fall two phases behind.
-        if (T0_COVERS_STEP && t == 0) {
-          if constexpr (ELEM == kE4M3) {
-            const int gv = g0 + j;  // V(j) converted; K(j+1) landed when there is a block j+1
-            if (!mbar_wait_warp(&v_ready[gv % ST], (gv / ST) & 1, abort_flag, p.status) ||
-                (j + 1 < w.n_blocks &&
-                 !mbar_wait_warp(&in_full[(gv + 1) % ST], ((gv + 1) / ST) & 1, abort_flag, p.status))) {
-              ok = false;
-              break;
-            }
-          } else {
-            const int g_next = g0 + j + 1;
-            if (!mbar_wait_warp(&in_full[g_next % ST], (g_next / ST) & 1, abort_flag, p.status)) {
-              ok = false;
-              break;
+              for (int i = 0; i < 32; i += 2) {
+                float a = __uint_as_float(o[i]), b = __uint_as_float(o[i + 1]);
+                fmul2_scalar(a, b, alpha);
+                o[i] = __float_as_uint(a);
+                o[i + 1] = __float_as_uint(b);
+              }
+              tmem_st32(tO + c * 32, o);
             }
           }
+          // P_0(j) also stands for what the MMA thread's step j+1 reads (V(j) among it, which the
+          // first half of P_0(j) V(j) already reads), so it skips its own waits at that step.
+          // Tile 0 is active in every work tile, and the MMA thread waits for itself at every
+          // step tile 0 does not cover, so these waits never fall two phases behind.
+          if (T0_COVERS_STEP && t == 0) {
+            if constexpr (ELEM == kE4M3) {
+              const int gv = g0 + j;  // V(j) converted; K(j+1) landed when there is a block j+1
+              if (!mbar_wait_warp(&v_ready[gv % ST], (gv / ST) & 1, abort_flag, p.status) ||
+                  (j + 1 < w.n_blocks &&
+                   !mbar_wait_warp(&in_full[(gv + 1) % ST], ((gv + 1) / ST) & 1, abort_flag, p.status))) {
+                ok = false;
+                break;
+              }
+            } else {
+              const int g_next = g0 + j + 1;
+              if (!mbar_wait_warp(&in_full[g_next % ST], (g_next / ST) & 1, abort_flag, p.status)) {
+                ok = false;
+                break;
+              }
+            }
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&p_half[t]);
         }
+        if (!ok) break;
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&p_full[t]);

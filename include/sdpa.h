@@ -307,10 +307,11 @@ int sdpa_decode_paged(const void* q, const void* k_pool, const void* v_pool, con
                       size_t workspace_bytes, sdpa_dtype dtype, void* stream);
 
 /*
- * sdpa_decode_noalloc -- sdpa_decode for callers that cannot allocate device memory: code
- * that runs while a CUDA graph is being captured, allocator-free runtimes, and hosts that
- * hand out device memory only through their own pool.  The pages this library follows have
- * no counterpart for it.
+ * sdpa_decode_noalloc -- sdpa_decode for callers that cannot allocate device memory: runtimes
+ * without a device allocator of their own, hosts that hand out device memory only through
+ * their own pool and forbid library allocations, and serving loops that must not call
+ * cudaMalloc on the hot path (it can synchronize the device).  The pages this library follows
+ * have no counterpart for it.
  *
  * Arguments and results are those of sdpa_decode without the workspace: the per-split
  * partials go to a fixed 32 MiB array in the library's own device memory, which every GPU

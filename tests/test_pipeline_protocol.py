@@ -100,11 +100,11 @@ def _run(units, stages, seed, tile1_on_released=False, p_half=False):
                     yield ("wait", bar(f"released{G % stages}"), G // stages)
                 else:
                     yield ("wait", bar(f"s_full{t}"), sn)
-                if p_half:
-                    yield ("do", bar(f"p_half{t}"))
                 if t == 0:
                     G = g0 + j + 1
                     yield ("wait", bar(f"in_full{G % stages}"), G // stages)
+                if p_half:  # after the covering wait: the first half of P.V reads V(j) already
+                    yield ("do", bar(f"p_half{t}"))
                 yield ("do", bar(f"p_full{t}"))
                 sn += 1
             yield ("wait", bar(f"o_full{t}"), on)
@@ -270,13 +270,13 @@ def _run_e4m3(units, stages, seed, t0_covers=True, p_half=False):
                 continue
             for j in range(nt[t]):
                 yield ("wait", bar(f"s_full{t}"), sn)
-                if p_half:
-                    yield ("do", bar(f"p_half{t}"))
                 if t == 0 and t0_covers:
                     G = g0 + j
                     yield ("wait", bar(f"v_ready{G % stages}"), G // stages)
                     if j + 1 < nb:
                         yield ("wait", bar(f"in_full{(G + 1) % stages}"), (G + 1) // stages)
+                if p_half:
+                    yield ("do", bar(f"p_half{t}"))
                 yield ("do", bar(f"p_full{t}"))
                 sn += 1
             yield ("wait", bar(f"o_full{t}"), on)

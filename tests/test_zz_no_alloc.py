@@ -1,6 +1,7 @@
 """sdpa_decode_noalloc, the decode entry point that allocates nothing.  It serves callers that
-cannot allocate device memory where they run attention: code inside a CUDA graph capture, or a
-host whose allocator hands out no memory to libraries.  Its partial results go to a fixed array
+cannot allocate device memory where they run attention: a runtime without a device allocator of
+its own, a host whose pool hands out no memory to libraries, or a serving loop that must not call
+cudaMalloc on its hot path.  Its partial results go to a fixed array
 inside the library instead of a caller workspace.  Through the C ABI its results must equal
 sdpa_decode's bit for bit (the same kernels on the same inputs), on two calls in a row that share
 the fixed array, and match the fp64 oracle.
