@@ -41,6 +41,9 @@ METRIC = "attention fwd TFLOP/s (prefill) & HBM GB/s (decode), % of GB300 roofli
 HEADLINE = "gqa_causal_prefill_bf16_d128"
 L2_FLUSH_BYTES = 256 << 20
 FP8_PER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor ratio (4.5 / 2.25 PFLOP/s)
+# dense e4m3 library GEMM measured on this GPU type with `python bench.py --tensor-peaks`
+# (torch._scaled_mm, 16384^3, best of 10): context beside the nominal-ratio FP8 peak
+FP8_MEASURED_TFLOPS = 3783.0
 
 
 # ----------------------------------------------------------------------------- work counts
@@ -256,6 +259,7 @@ def bench_prefill(w, K, W, dev, peaks, flusher):
         r["roofline"] = {"bound": "tensor", "achieved": tflops, "peak": fp8, "unit": "TFLOP/s", "frac": tflops / fp8,
                          "peak_note": "FP8 = measured bf16 burst x 2 (nominal ratio); of measured",
                          "mixed_ceiling": mixed, "frac_of_mixed_ceiling": tflops / mixed,
+                         "fp8_measured_peak": FP8_MEASURED_TFLOPS, "frac_of_measured_fp8": tflops / FP8_MEASURED_TFLOPS,
                          "traffic": recorded_traffic(w.name)}
     else:
         r["roofline"] = {"bound": "tensor", "achieved": tflops, "peak": bf16, "unit": "TFLOP/s", "frac": tflops / bf16,

@@ -226,7 +226,7 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
                                  : elem == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const CUtensorMapSwizzle sw_qk = elem == kE4M3 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
-  alignas(64) CUtensorMap tq, tk, tv;
+  alignas(64) CUtensorMap tq, tk, tv, to;
   const int mB = vl ? 1 : B, mSq = vl ? vl->total_q : Sq, mSk = vl ? vl->total_k : Sk;  // tensor-map extents
   if (!encode_bshd(&tq, q, dt, esize, mB, mSq, Hq, D, st[0], st[1], st[2], 64, kBlockQ, sw_qk)) return SDPA_ERR_CUDA;
   if (!encode_bshd(&tk, k, dt, esize, mB, mSk, Hkv, D, st[3], st[4], st[5], 64, kBlockK, sw_qk)) return SDPA_ERR_CUDA;
@@ -236,6 +236,11 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
                         : encode_bshd(&tv, v, dt, 2, mB, mSk, Hkv, Dv, st[6], st[7], st[8], 64, kBlockK,
                                       CU_TENSOR_MAP_SWIZZLE_128B);
   if (!v_ok) return SDPA_ERR_CUDA;
+  // O [B, Sq, Hq, Dv] in the output type, 64-column boxes of 128 rows (the epilogue's TMA stores;
+  // rows past Sq are clipped; packed sequences store row by row instead)
+  const CUtensorMapDataType odt = out_dtype == SDPA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!encode_bshd(&to, o, odt, 2, mB, mSq, Hq, Dv, st[9], st[10], st[11], 64, kBlockQ, CU_TENSOR_MAP_SWIZZLE_128B))
+    return SDPA_ERR_CUDA;
 
   uint32_t* status = nullptr;
   if (status_ptr(&status) != cudaSuccess) return SDPA_ERR_CUDA;
@@ -296,17 +301,17 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
     p.k_scale = i8->k_scale;
     p.v_scale = i8->v_scale;
     p.n_qblocks = (Sq + kBlockQ - 1) / kBlockQ;
-    e = elem == kBF16 ? launch_prefill_bf16_block_scaled(D, causal != 0, tq, tk, tv, p, stm, &supported)
-                      : launch_prefill_f16_block_scaled(D, causal != 0, tq, tk, tv, p, stm, &supported);
+    e = elem == kBF16 ? launch_prefill_bf16_block_scaled(D, causal != 0, tq, tk, tv, to, p, stm, &supported)
+                      : launch_prefill_f16_block_scaled(D, causal != 0, tq, tk, tv, to, p, stm, &supported);
     if (!supported) return SDPA_ERR_UNSUPPORTED;
     return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
   }
   if (elem == kE4M3)
-    e = launch_prefill_e4m3(D, Dv, causal != 0, mask != nullptr, tq, tk, tv, p, stm, &supported);
+    e = launch_prefill_e4m3(D, Dv, causal != 0, mask != nullptr, tq, tk, tv, to, p, stm, &supported);
   else if (elem == kBF16)
-    e = launch_prefill_bf16(D, Dv, causal != 0, mask != nullptr, tq, tk, tv, p, stm, &supported);
+    e = launch_prefill_bf16(D, Dv, causal != 0, mask != nullptr, tq, tk, tv, to, p, stm, &supported);
   else
-    e = launch_prefill_f16(D, Dv, causal != 0, mask != nullptr, tq, tk, tv, p, stm, &supported);
+    e = launch_prefill_f16(D, Dv, causal != 0, mask != nullptr, tq, tk, tv, to, p, stm, &supported);
   if (!supported) return SDPA_ERR_UNSUPPORTED;
   return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }

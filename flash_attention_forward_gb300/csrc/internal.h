@@ -28,6 +28,38 @@ enum ElemKind : int { kF16 = 0, kBF16 = 1, kE4M3 = 2 };
 // may be scaled per channel.
 enum PrefillVariant : int { kDense = 0, kVarlen = 1, kBlockScaled = 2 };
 
+// Division by a launch constant d >= 1 with one multiply-high, two adds and two shifts, exact
+// for every 32-bit numerator (the unsigned scheme of Granlund and Montgomery, "Division by
+// Invariant Integers using Multiplication", 1994, figure 4.1): with l = ceil(log2 d) and
+// m = floor(2^32 (2^l - d) / d) + 1, t = umulhi(m, n) and n / d = (t + ((n - t) >> min(l, 1)))
+// >> max(l - 1, 0).  The work-tile decode runs on the single MMA-issuing thread and on every
+// softmax warp at each new work tile, where a general integer division costs tens of
+// instructions; 32-bit arithmetic keeps it from holding register pairs.
+struct FastDiv {
+  uint32_t m = 1, sh1 = 0, sh2 = 0;
+  uint32_t d = 1;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f;
+  uint32_t l = 0;
+  while ((uint64_t(1) << l) < d) ++l;  // l <= 31 for d < 2^31
+  f.m = static_cast<uint32_t>(((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1);
+  f.sh1 = l < 1 ? l : 1;
+  f.sh2 = l > 1 ? l - 1 : 0;
+  f.d = d;
+  return f;
+}
+#ifdef __CUDACC__
+__host__ __device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv& f) {
+#ifdef __CUDA_ARCH__
+  const uint32_t t = __umulhi(f.m, n);
+#else
+  const uint32_t t = static_cast<uint32_t>((static_cast<uint64_t>(f.m) * n) >> 32);
+#endif
+  return (t + ((n - t) >> f.sh1)) >> f.sh2;
+}
+#endif
+
 struct PrefillParams {
   void* o;                 // [B, Sq, Hq, Dv] out dtype
   float* lse;              // [B, Hq, Sq] or null
@@ -38,6 +70,9 @@ struct PrefillParams {
   int group;               // Hq / Hkv
   int n_cta_tiles;         // ceil(Sq / kCtaRows)
   int units_per_group;     // KV units (batch x KV head) whose work tiles are scheduled together
+  // divisors of the work-tile decode: a full group's work tiles, a row band of a full group and of
+  // the last group, the query heads per KV head, Hkv (dense) or Hq (packed sequences)
+  FastDiv div_gsize, div_band, div_band_last, div_group, div_heads;
   int n_kblocks;           // ceil(Sk / kBlockK)
   float scale2;            // scale * log2(e) (times descale_q * descale_k for e4m3)
   float inv_scale;         // 1 / (scale * descale_q * descale_k): mask values enter s in score units
@@ -156,22 +191,23 @@ struct WidenParams {
   int to_bf16;             // 1: bf16 copies, 0: f16
 };
 
-// Kernel launchers (return cudaError_t of the launch).  The prefill launchers set
-// *supported = false (and launch nothing) for head dims they were not built for.
+// Kernel launchers (return cudaError_t of the launch).  The prefill launchers take the tensor
+// maps of Q, K, V and O and set *supported = false (and launch nothing) for head dims they were
+// not built for.
 cudaError_t launch_prefill_f16(int D, int Dv, bool causal, bool has_mask, const CUtensorMap& tq,
-                               const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st,
+                               const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to, const PrefillParams& p, cudaStream_t st,
                                bool* supported);
 cudaError_t launch_prefill_bf16(int D, int Dv, bool causal, bool has_mask, const CUtensorMap& tq,
-                                const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st,
+                                const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to, const PrefillParams& p, cudaStream_t st,
                                 bool* supported);
 cudaError_t launch_prefill_f16_block_scaled(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
-                                           const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st,
+                                           const CUtensorMap& tv, const CUtensorMap& to, const PrefillParams& p, cudaStream_t st,
                                            bool* supported);
 cudaError_t launch_prefill_bf16_block_scaled(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
-                                            const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st,
+                                            const CUtensorMap& tv, const CUtensorMap& to, const PrefillParams& p, cudaStream_t st,
                                             bool* supported);
 cudaError_t launch_prefill_e4m3(int D, int Dv, bool causal, bool has_mask, const CUtensorMap& tq,
-                                const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st,
+                                const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to, const PrefillParams& p, cudaStream_t st,
                                 bool* supported);
 
 cudaError_t launch_decode(int elem, int D, const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -57,7 +57,12 @@ struct PrefillCfg {
   static constexpr int OFF_K = OFF_Q + kTilesPerCta * Q_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * K_BYTES;
   static constexpr int OFF_VRAW = OFF_V + STAGES * V_BYTES;
-  static constexpr int OFF_BAR = OFF_VRAW + STAGES * VRAW_BYTES;
+  // output staging of the 16-bit kernels: one 64-column box of 16-bit rows (128 x 128 B) per
+  // softmax warpgroup (the e4m3 kernels store O row by row: measured faster there)
+  static constexpr bool TMA_EPILOGUE = ELEM != kE4M3;
+  static constexpr int OST_BYTES = TMA_EPILOGUE ? kBlockQ * 128 : 0;
+  static constexpr int OFF_OST = OFF_VRAW + STAGES * VRAW_BYTES;
+  static constexpr int OFF_BAR = OFF_OST + kTilesPerCta * OST_BYTES;
   // barriers, tmem base, abort flag; then 1 KB of slack so that the 1024-B alignment of the
   // dynamic shared window never pushes the last byte past the allocation
   static constexpr int SMEM = OFF_BAR + 512 + 1024;
@@ -157,7 +162,11 @@ __device__ __forceinline__ int64_t lse_index(const PrefillParams& p, const WorkT
 // K/V fits in L2), so the K/V that the CTAs running at the same time need stays resident in L2.
 // Inside a group, causal tiles at the bottom of the matrix see the most keys and come first;
 // tiles of one row band are ordered by unit, then query head.
-template <bool CAUSAL, bool VARLEN>
+// FAST: divide by the launch constants with precomputed reciprocals.  Every role decodes every
+// work tile, the single MMA-issuing thread included, for which the decode is pure overhead
+// between MMA groups.  The masked kernels divide plainly: with the reciprocals their softmax
+// spills (measured slower there, faster on the unmasked kernels).
+template <bool CAUSAL, bool VARLEN, bool FAST = true>
 __device__ __forceinline__ WorkTile work_tile(const PrefillParams& p, int work_unit) {
   WorkTile w;
   w.split = -1, w.part = 0, w.jb0 = 0;
@@ -166,9 +175,9 @@ __device__ __forceinline__ WorkTile work_tile(const PrefillParams& p, int work_u
     // unit = (tile of the packed sequences) * Hq + head; a sequence's tiles run longest first
     // when causal.  Units past the last tile are empty.
     const int total_tiles = __ldg(p.tile_prefix + p.B);
-    const int tg = work_unit / p.Hq;
+    const int tg = FAST ? static_cast<int>(fast_div(static_cast<uint32_t>(work_unit), p.div_heads)) : work_unit / p.Hq;
     w.h = work_unit - tg * p.Hq;
-    w.kvh = w.h / p.group;
+    w.kvh = FAST ? static_cast<int>(fast_div(static_cast<uint32_t>(w.h), p.div_group)) : w.h / p.group;
     if (tg >= total_tiles) {
       w.b = 0, w.q0 = 0, w.sq = 0, w.sk = 0, w.q_off = 0, w.k_off = 0, w.cb = 0;
       w.n_t[0] = w.n_t[1] = 0;
@@ -193,31 +202,37 @@ __device__ __forceinline__ WorkTile work_tile(const PrefillParams& p, int work_u
     jb1 = max(1, (w.sk + kBlockK - 1) / kBlockK);
   } else {
     // work units past the whole work tiles are key ranges of the split tail (never causal)
-    int item = work_unit, parts = 1;
+    int item = work_unit;
     if (!CAUSAL && work_unit >= p.n_full) {
       const int r = work_unit - p.n_full;
-      parts = p.split_parts;
+      const int parts = p.split_parts;
       w.split = r / parts;
       w.part = r - w.split * parts;
       item = p.n_full + w.split;
+      w.jb0 = w.part * p.n_kblocks / parts;
+      jb1 = (w.part + 1) * p.n_kblocks / parts;
     }
-    w.jb0 = w.part * p.n_kblocks / parts;
-    jb1 = (w.part + 1) * p.n_kblocks / parts;
     const int G = p.group;                           // query heads per KV head
     const int units = p.B * p.Hkv;
-    const int per_unit = G * p.n_cta_tiles;          // work tiles of one KV unit
-    const int gsize = p.units_per_group * per_unit;  // work tiles of a full group
-    const int gi = item / gsize;
+    const int gsize = static_cast<int>(p.div_gsize.d);  // work tiles of a full group
+    const int gi = FAST ? static_cast<int>(fast_div(static_cast<uint32_t>(item), p.div_gsize)) : item / gsize;
     const int base = gi * p.units_per_group;
-    const int ul = min(p.units_per_group, units - base);  // units in this group (last may be short)
+    const bool last = units - base < p.units_per_group;  // the last group may hold fewer units
+    FastDiv band;
+    band.m = last ? p.div_band_last.m : p.div_band.m;
+    band.sh1 = last ? p.div_band_last.sh1 : p.div_band.sh1;
+    band.sh2 = last ? p.div_band_last.sh2 : p.div_band.sh2;
+    band.d = last ? p.div_band_last.d : p.div_band.d;
     const int r = item - gi * gsize;
-    const int rank = r / (ul * G);                   // row band, longest first when causal
-    const int q = r - rank * (ul * G);
-    const int unit = base + q / G;
+    // row band, longest first when causal
+    const int rank = FAST ? static_cast<int>(fast_div(static_cast<uint32_t>(r), band)) : r / static_cast<int>(band.d);
+    const int q = r - rank * static_cast<int>(band.d);
+    const int qg = FAST ? static_cast<int>(fast_div(static_cast<uint32_t>(q), p.div_group)) : q / G;
+    const int unit = base + qg;
     const int ctile = CAUSAL ? (p.n_cta_tiles - 1 - rank) : rank;
-    w.b = unit / p.Hkv;
-    w.kvh = unit % p.Hkv;
-    w.h = w.kvh * G + q % G;
+    w.b = FAST ? static_cast<int>(fast_div(static_cast<uint32_t>(unit), p.div_heads)) : unit / p.Hkv;
+    w.kvh = unit - w.b * p.Hkv;
+    w.h = w.kvh * G + (q - qg * G);
     w.q0 = ctile * kCtaRows;
     w.sq = p.Sq, w.sk = p.Sk;
     w.q_off = 0, w.k_off = 0, w.cb = w.b;
@@ -270,7 +285,8 @@ __device__ __forceinline__ int nth_item(int k) {
 template <int ELEM, int D, int DV, bool CAUSAL, bool MASK, int VAR>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                   const PrefillParams p) {
   using C = PrefillCfg<ELEM, D, DV>;
   constexpr bool VARLEN = VAR == kVarlen;
   constexpr bool SCALED = VAR == kBlockScaled;
@@ -278,6 +294,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   // signals P_0(j) (16-bit: ring step j+1 landed; e4m3: V(j) converted and K(j+1) landed), which
   // spares the MMA thread those waits (with a mask the longer softmax would then hold it up)
   constexpr bool T0_COVERS_STEP = !MASK;
+  constexpr bool FAST_DIV = !MASK;
   constexpr int ST = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -352,7 +369,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       int g = 0;           // ring steps issued
       bool ok = true;
       for (int k = 0, item = nth_item(0); ok && item < n_items; item = nth_item(++k)) {
-        const WorkTile w = work_tile<CAUSAL, VARLEN>(p, item);
+        const WorkTile w = work_tile<CAUSAL, VARLEN, FAST_DIV>(p, item);
         if (VARLEN && w.n_blocks == 0) continue;  // an empty unit (past the packed sequences' tiles)
         for (int t = 0; t < kTilesPerCta && ok; ++t) {
           if (w.n_t[t] == 0) continue;
@@ -444,7 +461,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       int g = 0;            // ring steps consumed
       bool ok = true;
       for (int k = 0, item = nth_item(0); ok && item < n_items; item = nth_item(++k)) {
-        const WorkTile w = work_tile<CAUSAL, VARLEN>(p, item);
+        const WorkTile w = work_tile<CAUSAL, VARLEN, FAST_DIV>(p, item);
         if (VARLEN && w.n_blocks == 0) continue;  // an empty unit: skipped by every role
         for (int t = 0; t < kTilesPerCta && ok; ++t)
           if (w.n_t[t] > 0) ok = mbar_wait(&q_full[t], qn[t] & 1, abort_flag, p.status);
@@ -621,7 +638,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       int g = 0;
       bool ok = true;
       for (int k = 0, item = nth_item(0); ok && item < n_items; item = nth_item(++k)) {
-        const WorkTile w = work_tile<CAUSAL, VARLEN>(p, item);
+        const WorkTile w = work_tile<CAUSAL, VARLEN, FAST_DIV>(p, item);
         for (int j = 0; j < w.n_blocks; ++j, ++g) {
           const int s = g % ST, r = g / ST;
           if (!mbar_wait(&v_full[s], r & 1, abort_flag, p.status)) {
@@ -660,13 +677,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem_base + lane_off + t * 128;
     const uint32_t tO = tmem_base + lane_off + 256 + t * 128;
+    const bool wg_leader = wq == 0 && lane == 0;  // issues this warpgroup's output stores
     const float scale2 = p.scale2;
     int sn = 0;     // S blocks consumed (s_full / p_full phases)
     int on = 0;     // work tiles finished (o_full phases)
     int gbase = 0;  // ring index of the current work tile's first step (tile 0 uses it)
     bool ok = true;
     for (int k = 0, item = nth_item(0); ok && item < n_items; item = nth_item(++k)) {
-      const WorkTile w = work_tile<CAUSAL, VARLEN>(p, item);
+      const WorkTile w = work_tile<CAUSAL, VARLEN, FAST_DIV>(p, item);
       const int g0 = gbase;
       // every role skips empty units; the 16-bit ring takes n_blocks + 1 steps, e4m3 n_blocks
       gbase += w.n_blocks > 0 ? w.n_blocks + (ELEM == kE4M3 ? 0 : 1) : 0;
@@ -885,40 +903,93 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       const float* vs_row = nullptr;  // int8 V codes: per-channel scales
       if constexpr (SCALED)
         if (p.v_scale != nullptr) vs_row = p.v_scale + (static_cast<int64_t>(w.b) * p.Hkv + w.kvh) * DV;
+      if constexpr (!VARLEN && C::TMA_EPILOGUE) {
+        // O leaves through shared memory: each 64-column half of the tile goes to this
+        // warpgroup's staging box (128-byte swizzle, conflict-free rows) and out by one TMA store,
+        // which writes whole rows of global memory (rows past Sq clipped) and runs on while the
+        // warpgroup starts its next work tile.  A thread storing its own row straight from
+        // registers writes 16-byte pieces of 32 rows per instruction instead.
+        uint8_t* ost = smem + C::OFF_OST + t * C::OST_BYTES;
 #pragma unroll 1
-      for (int c = 0; c < DV / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tO + c * 32, o);
-        tmem_ld_wait();
-        reg_fence(o);
-        if constexpr (SCALED) {
-          if (vs_row != nullptr) {
+        for (int hb = 0; hb < DV / 64; ++hb) {
+          // the staging box is free once the previous store from it has read it
+          if (wg_leader) bulk_wait_read_all();
+          named_barrier_sync(1 + t, 128);
+#pragma unroll 1
+          for (int cc = 0; cc < 2; ++cc) {
+            const int c = 2 * hb + cc;
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_ld_wait();
+            reg_fence(o);
+            if constexpr (SCALED) {
+              if (vs_row != nullptr) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float4 f = __ldg(reinterpret_cast<const float4*>(vs_row + c * 32) + i);
-              o[4 * i] = __float_as_uint(__uint_as_float(o[4 * i]) * f.x);
-              o[4 * i + 1] = __float_as_uint(__uint_as_float(o[4 * i + 1]) * f.y);
-              o[4 * i + 2] = __float_as_uint(__uint_as_float(o[4 * i + 2]) * f.z);
-              o[4 * i + 3] = __float_as_uint(__uint_as_float(o[4 * i + 3]) * f.w);
+                for (int i = 0; i < 8; ++i) {
+                  const float4 f = __ldg(reinterpret_cast<const float4*>(vs_row + c * 32) + i);
+                  o[4 * i] = __float_as_uint(__uint_as_float(o[4 * i]) * f.x);
+                  o[4 * i + 1] = __float_as_uint(__uint_as_float(o[4 * i + 1]) * f.y);
+                  o[4 * i + 2] = __float_as_uint(__uint_as_float(o[4 * i + 2]) * f.z);
+                  o[4 * i + 3] = __float_as_uint(__uint_as_float(o[4 * i + 3]) * f.w);
+                }
+              }
             }
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack_out<ELEM>(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              *reinterpret_cast<uint4*>(ost + row * 128 + (((4 * cc + i) ^ (row & 7)) << 4)) =
+                  make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+          fence_proxy_async_smem();
+          named_barrier_sync(1 + t, 128);
+          if (wg_leader) {
+            tma_store_4d(&tm_o, ost, hb * 64, w.h, w.q_off + w.q0 + t * kBlockQ, w.cb);
+            bulk_commit_group();
           }
         }
-        uint32_t pk[16];
+      } else {
+        // packed sequences (a tile's rows past its sequence belong to the next one) and the e4m3
+        // kernels: each thread stores its own row
+#pragma unroll 1
+        for (int c = 0; c < DV / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_ld_wait();
+          reg_fence(o);
+          if constexpr (SCALED) {
+            if (vs_row != nullptr) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_out<ELEM>(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
-        if (row_valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 64);
+              for (int i = 0; i < 8; ++i) {
+                const float4 f = __ldg(reinterpret_cast<const float4*>(vs_row + c * 32) + i);
+                o[4 * i] = __float_as_uint(__uint_as_float(o[4 * i]) * f.x);
+                o[4 * i + 1] = __float_as_uint(__uint_as_float(o[4 * i + 1]) * f.y);
+                o[4 * i + 2] = __float_as_uint(__uint_as_float(o[4 * i + 2]) * f.z);
+                o[4 * i + 3] = __float_as_uint(__uint_as_float(o[4 * i + 3]) * f.w);
+              }
+            }
+          }
+          uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_out<ELEM>(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+          if (row_valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 64);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+          __syncwarp();
         }
-        __syncwarp();
       }
       // O_t has been read: the next work tile's first P.V may overwrite it
       tc_fence_before();
       mbar_arrive(&o_empty[t]);
       if (lse_out != nullptr && row_valid) *lse_out = (l > 0.f) ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
     }
+    // the shared-memory staging must outlive every output store issued from it
+    if (wg_leader) bulk_wait_all();
   }
 
   tc_fence_before();

@@ -6,22 +6,22 @@
 namespace sdpa {
 
 cudaError_t launch_prefill_bf16(int D, int Dv, bool causal, bool has_mask, const CUtensorMap& tq,
-                                const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st,
+                                const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to, const PrefillParams& p, cudaStream_t st,
                                 bool* supported) {
   *supported = true;
-  if (D == 64 && Dv == 64) return launch_prefill_dims<kBF16, 64, 64>(causal, has_mask, tq, tk, tv, p, st);
-  if (D == 128 && Dv == 128) return launch_prefill_dims<kBF16, 128, 128>(causal, has_mask, tq, tk, tv, p, st);
-  if (D == 192 && Dv == 128) return launch_prefill_dims<kBF16, 192, 128>(causal, has_mask, tq, tk, tv, p, st);
+  if (D == 64 && Dv == 64) return launch_prefill_dims<kBF16, 64, 64>(causal, has_mask, tq, tk, tv, to, p, st);
+  if (D == 128 && Dv == 128) return launch_prefill_dims<kBF16, 128, 128>(causal, has_mask, tq, tk, tv, to, p, st);
+  if (D == 192 && Dv == 128) return launch_prefill_dims<kBF16, 192, 128>(causal, has_mask, tq, tk, tv, to, p, st);
   *supported = false;
   return cudaSuccess;
 }
 
 cudaError_t launch_prefill_bf16_block_scaled(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
-                                      const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st,
+                                      const CUtensorMap& tv, const CUtensorMap& to, const PrefillParams& p, cudaStream_t st,
                                       bool* supported) {
   *supported = true;
-  if (D == 64) return launch_prefill_block_scaled<kBF16, 64>(causal, tq, tk, tv, p, st);
-  if (D == 128) return launch_prefill_block_scaled<kBF16, 128>(causal, tq, tk, tv, p, st);
+  if (D == 64) return launch_prefill_block_scaled<kBF16, 64>(causal, tq, tk, tv, to, p, st);
+  if (D == 128) return launch_prefill_block_scaled<kBF16, 128>(causal, tq, tk, tv, to, p, st);
   *supported = false;
   return cudaSuccess;
 }

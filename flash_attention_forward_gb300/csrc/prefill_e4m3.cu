@@ -5,12 +5,12 @@
 namespace sdpa {
 
 cudaError_t launch_prefill_e4m3(int D, int Dv, bool causal, bool has_mask, const CUtensorMap& tq,
-                                const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st,
+                                const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to, const PrefillParams& p, cudaStream_t st,
                                 bool* supported) {
   *supported = true;
-  if (D == 64 && Dv == 64) return launch_prefill_dims<kE4M3, 64, 64>(causal, has_mask, tq, tk, tv, p, st);
-  if (D == 128 && Dv == 128) return launch_prefill_dims<kE4M3, 128, 128>(causal, has_mask, tq, tk, tv, p, st);
-  if (D == 192 && Dv == 128) return launch_prefill_dims<kE4M3, 192, 128>(causal, has_mask, tq, tk, tv, p, st);
+  if (D == 64 && Dv == 64) return launch_prefill_dims<kE4M3, 64, 64>(causal, has_mask, tq, tk, tv, to, p, st);
+  if (D == 128 && Dv == 128) return launch_prefill_dims<kE4M3, 128, 128>(causal, has_mask, tq, tk, tv, to, p, st);
+  if (D == 192 && Dv == 128) return launch_prefill_dims<kE4M3, 192, 128>(causal, has_mask, tq, tk, tv, to, p, st);
   *supported = false;
   return cudaSuccess;
 }

@@ -6,7 +6,7 @@
 namespace sdpa {
 
 template <int ELEM, int D, int DV, bool CAUSAL, bool MASK, int VAR>
-cudaError_t launch_prefill_instance(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+cudaError_t launch_prefill_instance(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                                     const PrefillParams& p, cudaStream_t st) {
   using C = PrefillCfg<ELEM, D, DV>;
   auto kern = prefill_kernel<ELEM, D, DV, CAUSAL, MASK, VAR>;
@@ -32,6 +32,15 @@ cudaError_t launch_prefill_instance(const CUtensorMap& tq, const CUtensorMap& tk
   long long ug = aligned < cap ? aligned : cap;
   const long long kv_units = (long long)p.B * p.Hkv;
   q.units_per_group = (int)(ug < 1 ? 1 : (ug > kv_units ? kv_units : ug));
+  {
+    const long long G = p.group, upg = q.units_per_group;
+    const long long last_units = kv_units - (kv_units - 1) / upg * upg;  // units of the last group
+    q.div_gsize = make_fastdiv((uint32_t)(upg * G * p.n_cta_tiles));
+    q.div_band = make_fastdiv((uint32_t)(upg * G));
+    q.div_band_last = make_fastdiv((uint32_t)(last_units * G));
+    q.div_group = make_fastdiv((uint32_t)G);
+    q.div_heads = make_fastdiv((uint32_t)(VAR == kVarlen ? p.Hq : p.Hkv));
+  }
   // Programmatic dependent launch where the previous kernel of the stream is this library's own:
   // the masked prefill after mask_convert_kernel (only its softmax reads what that kernel
   // writes, after griddepcontrol.wait), and the split merge after the prefill.
@@ -46,9 +55,9 @@ cudaError_t launch_prefill_instance(const CUtensorMap& tq, const CUtensorMap& tk
     cfg.stream = st;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
-    if ((e = cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, q)) != cudaSuccess) return e;
+    if ((e = cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, to, q)) != cudaSuccess) return e;
   } else {
-    kern<<<grid, kPrefillThreads, C::SMEM, st>>>(tq, tk, tv, q);
+    kern<<<grid, kPrefillThreads, C::SMEM, st>>>(tq, tk, tv, to, q);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (!CAUSAL && VAR != kVarlen && p.split_parts > 1) {
@@ -67,23 +76,23 @@ cudaError_t launch_prefill_instance(const CUtensorMap& tq, const CUtensorMap& tk
 
 template <int ELEM, int D, int DV>
 cudaError_t launch_prefill_dims(bool causal, bool has_mask, const CUtensorMap& tq, const CUtensorMap& tk,
-                                const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st) {
+                                const CUtensorMap& tv, const CUtensorMap& to, const PrefillParams& p, cudaStream_t st) {
   if (p.varlen)  // packed sequences: no mask, no split tail
-    return causal ? launch_prefill_instance<ELEM, D, DV, true, false, kVarlen>(tq, tk, tv, p, st)
-                  : launch_prefill_instance<ELEM, D, DV, false, false, kVarlen>(tq, tk, tv, p, st);
+    return causal ? launch_prefill_instance<ELEM, D, DV, true, false, kVarlen>(tq, tk, tv, to, p, st)
+                  : launch_prefill_instance<ELEM, D, DV, false, false, kVarlen>(tq, tk, tv, to, p, st);
   if (causal)
-    return has_mask ? launch_prefill_instance<ELEM, D, DV, true, true, kDense>(tq, tk, tv, p, st)
-                    : launch_prefill_instance<ELEM, D, DV, true, false, kDense>(tq, tk, tv, p, st);
-  return has_mask ? launch_prefill_instance<ELEM, D, DV, false, true, kDense>(tq, tk, tv, p, st)
-                  : launch_prefill_instance<ELEM, D, DV, false, false, kDense>(tq, tk, tv, p, st);
+    return has_mask ? launch_prefill_instance<ELEM, D, DV, true, true, kDense>(tq, tk, tv, to, p, st)
+                    : launch_prefill_instance<ELEM, D, DV, true, false, kDense>(tq, tk, tv, to, p, st);
+  return has_mask ? launch_prefill_instance<ELEM, D, DV, false, true, kDense>(tq, tk, tv, to, p, st)
+                  : launch_prefill_instance<ELEM, D, DV, false, false, kDense>(tq, tk, tv, to, p, st);
 }
 
 // int8 codes widened to 16 bits (Q/K/V already in the 16-bit type), per-block score scales.
 template <int ELEM, int D>
 cudaError_t launch_prefill_block_scaled(bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
-                                        const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st) {
-  return causal ? launch_prefill_instance<ELEM, D, D, true, false, kBlockScaled>(tq, tk, tv, p, st)
-                : launch_prefill_instance<ELEM, D, D, false, false, kBlockScaled>(tq, tk, tv, p, st);
+                                        const CUtensorMap& tv, const CUtensorMap& to, const PrefillParams& p, cudaStream_t st) {
+  return causal ? launch_prefill_instance<ELEM, D, D, true, false, kBlockScaled>(tq, tk, tv, to, p, st)
+                : launch_prefill_instance<ELEM, D, D, false, false, kBlockScaled>(tq, tk, tv, to, p, st);
 }
 
 }  // namespace sdpa
