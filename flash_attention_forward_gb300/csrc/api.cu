@@ -338,7 +338,7 @@ int decode_check(const void* q, const void* k, const void* v, const int32_t* pag
   if (paged && page_size < 16) return SDPA_ERR_UNSUPPORTED;
   const int group = Hq / Hkv;
   if (group > 16) return SDPA_ERR_UNSUPPORTED;  // one 16-row tensor-core tile per KV head
-  if (B > 65535 || Hkv > 65535) return SDPA_ERR_UNSUPPORTED;
+  if (B > 65535 || Hkv > 65535) return SDPA_ERR_UNSUPPORTED;  // launch-grid y and z extents
   // element strides {q_b, q_h, k_b, k_s, k_h, v_b, v_s, v_h, o_b, o_h} (+ page-table row stride)
   int64_t st[SDPA_DECODE_PAGED_NSTRIDES];
   const int rows = paged ? page_size : max_kv;  // rows of one batch entry of the caches

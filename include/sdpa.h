@@ -273,8 +273,11 @@ size_t sdpa_decode_workspace_size(int B, int Hq, int max_kv, int Dv);
  *           aligned, device memory; its contents on entry do not matter.
  *   dtype:  SDPA_F16 or SDPA_BF16.
  *
- * Supported: D = Dv = 128 and 1 <= Hq/Hkv <= 8; pointers 16-byte aligned; s/h/b strides
- * multiples of 8 elements.
+ * Supported: (D, Dv) in {(128, 128), (192, 128)} (the second is the MLA head shape of page
+ * "MlaMmaOp"); 1 <= Hq/Hkv <= 16 (all query heads of a KV head share one 16-row tensor-core tile,
+ * so every K/V byte is read once; section "GQA layout" of the Xe2 page leaves the group size
+ * open); B <= 65535 and Hkv <= 65535 (launch-grid limits); pointers 16-byte
+ * aligned; s/h/b strides multiples of 8 elements.  Otherwise SDPA_ERR_UNSUPPORTED.
  */
 int sdpa_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* kv_len, void* o, float* lse,
                 int B, int Hq, int Hkv, int max_kv, int D, int Dv, const int64_t* strides, float scale,
