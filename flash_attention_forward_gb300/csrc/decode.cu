@@ -137,6 +137,9 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const __grid_
   uint64_t* empty = full + ST;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + ST);
 
+  // the combine kernel may be scheduled once every CTA here has started; it waits for this
+  // grid's completion before it reads the partials
+  pdl_launch_dependents();
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int L = min(max(__ldg(p.kv_len + b), 0), p.max_kv);
@@ -401,6 +404,7 @@ __global__ void __launch_bounds__(kDecodeDv) decode_combine_kernel(const DecodeP
   constexpr int kPart = kDecodeDv + 2;  // floats per partial: O, then max, then sum
   constexpr int kGroup = 8;             // partials whose loads are in flight together
   const float* base = p.ws + (int64_t)(b * p.Hq + h) * p.n_splits_max * kPart;
+  pdl_wait();  // the partials come from the split kernel launched before
   float M = -INFINITY;
   for (int s0 = 0; s0 < ns; s0 += kGroup) {
     float m[kGroup];
@@ -568,17 +572,26 @@ cudaError_t launch_split(dim3 grid, const CUtensorMap& tk, const CUtensorMap& tv
 
 cudaError_t launch_decode(int elem, int D, const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                           cudaStream_t st) {
-  const dim3 g1(p.n_splits_max, p.Hkv, p.B), g2(p.Hq, p.B);
+  const dim3 g1(p.n_splits_max, p.Hkv, p.B);
   cudaError_t e;
-  if (elem == kBF16) {
+  if (elem == kBF16)
     e = D == 192 ? launch_split<kBF16, 192>(g1, tk, tv, p, st) : launch_split<kBF16, 128>(g1, tk, tv, p, st);
-    if (e != cudaSuccess) return e;
-    decode_combine_kernel<kBF16><<<g2, kDecodeDv, 0, st>>>(p);
-  } else {
+  else
     e = D == 192 ? launch_split<kF16, 192>(g1, tk, tv, p, st) : launch_split<kF16, 128>(g1, tk, tv, p, st);
-    if (e != cudaSuccess) return e;
-    decode_combine_kernel<kF16><<<g2, kDecodeDv, 0, st>>>(p);
-  }
+  if (e != cudaSuccess) return e;
+  // programmatic dependent launch: the combine's CTAs are scheduled while the split grid drains
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.Hq, p.B);
+  cfg.blockDim = dim3(kDecodeDv);
+  cfg.stream = st;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  e = elem == kBF16 ? cudaLaunchKernelEx(&cfg, decode_combine_kernel<kBF16>, p)
+                    : cudaLaunchKernelEx(&cfg, decode_combine_kernel<kF16>, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -30,9 +30,9 @@
  *  - Validation happens before any CUDA call; an invalid call launches nothing.
  *  - The library allocates no device memory in these entry points.  Decode and masked
  *    prefill take a caller workspace sized by the *_workspace_size functions.
- *  - sdpa_fwd, sdpa_fwd_fp8, sdpa_fwd_varlen*, sdpa_fwd_int8 and sdpa_decode* may be recorded
- *    into a CUDA graph (stream capture) once a first call on the device has run outside the
- *    capture; sdpa_fwd_host may not.
+ *  - sdpa_fwd, sdpa_fwd_fp8, sdpa_fwd_varlen*, sdpa_fwd_int8, sdpa_decode and
+ *    sdpa_decode_paged may be recorded into a CUDA graph (stream capture) once a first call on
+ *    the device has run outside the capture; sdpa_fwd_host may not.
  */
 #ifndef SDPA_GB300_H
 #define SDPA_GB300_H

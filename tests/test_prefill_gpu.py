@@ -191,6 +191,29 @@ def test_strided_views_and_broadcast_mask():
     assert_lse_close(lse.cpu().numpy(), ref_lse)
 
 
+@pytest.mark.parametrize("Sk,first", [(5, 3), (1100, 1), (2100, 7), (1031, 0)])
+def test_mask_views_at_every_alignment(Sk, first):
+    # the mask as a window of a wider buffer: rows start at every 2-byte offset from a 16-byte
+    # boundary (row 0 too, when `first` is odd), so the condensing reads key by key at the row
+    # edges and shifts the 16-byte chunks between them; Sk = 1100 and 2100 span several groups
+    # of 1024 keys, and some rows hold finite non-zero values
+    B, Sq, H = 2, 70, 2
+    x = workloads.custom_prefill(B, H, H, Sq, Sk, 64, 64, dtype="f16", seed=Sk + first)
+    g = torch.Generator().manual_seed(Sk)
+    wide = torch.where(torch.rand((B, Sq, Sk + 13), generator=g) < 0.3, float("-inf"), 0.0).to(torch.float16)
+    wide[:, :, first] = 0  # the first key of every row stays visible
+    wide[:, 5:9, first + Sk // 2] = 1.5
+    m = wide[:, :, first:first + Sk]
+    x["mask"] = m.contiguous()
+    q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
+    o, lse = fa.sdpa_fwd(q, k, v, scale=0.125, causal=False, mask=wide.to(DEV)[:, :, first:first + Sk])
+    torch.cuda.synchronize()
+    assert fa.sdpa_check_device_status() == fa.SDPA_OK
+    ref_o, ref_lse = oracle.sdpa_fwd(x["q"], x["k"], x["v"], x["mask"], scale=0.125)
+    assert_close(o.float().cpu().numpy(), ref_o, TOL_16BIT)
+    assert_lse_close(lse.cpu().numpy(), ref_lse, TOL_LSE_F16)
+
+
 def test_output_canaries_untouched():
     # O written into the middle of a larger buffer: the padding around it must stay as it was
     B, Sq, Sk, H, D = 1, 130, 200, 2, 64
