@@ -94,15 +94,6 @@ __device__ __forceinline__ uint32_t pack_p(float lo, float hi) {
     return pack_f16x2(lo, hi);
 }
 
-// (acc0, acc1) += the two rounded probabilities packed in w, exactly as the P.V product sees them
-template <int ELEM>
-__device__ __forceinline__ void acc_p_pair(float& acc0, float& acc1, uint32_t w) {
-  if constexpr (ELEM == kBF16)
-    add_bf16x2_to_f32(acc0, acc1, w);
-  else
-    add_f16x2_to_f32(acc0, acc1, w);
-}
-
 // Output element packing (bf16 unless the inputs are f16).
 template <int ELEM>
 __device__ __forceinline__ uint32_t pack_out(float lo, float hi) {
@@ -792,10 +783,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           l *= alpha;
           m_used = m_cand;
         }
-        // P = exp2(blk_scale2 * s - m), rounded to 16 bits; l sums the rounded values.  P goes to
-        // tensor memory in two halves of 64 keys, each signalled as soon as it is written
-        // (p_half, then p_full), so that the MMA thread starts P.V on the first half while the
-        // second is computed.
+        // P = exp2(blk_scale2 * s - m), rounded to 16 bits for the P.V product; l sums the fp32
+        // values, two at a time by one packed add (one instruction a pair, against two for
+        // sums of the rounded values).  P goes to tensor memory in two halves of 64 keys, each
+        // signalled as soon as it is written (p_half, then p_full), so that the MMA thread
+        // starts P.V on the first half while the second is computed.
         const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -806,11 +798,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             const int c = half * 64 + 2 * w2;
             float x0, x1;
             ffma2_scalar(x0, x1, s[c], s[c + 1], blk_scale2, neg_m);
-            pk[w2] = pack_p<ELEM>(ex2(x0), ex2(x1));
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            pk[w2] = pack_p<ELEM>(p0, p1);
             if (w2 & 1)
-              acc_p_pair<ELEM>(ls[2], ls[3], pk[w2]);
+              fadd2(ls[2], ls[3], p0, p1);
             else
-              acc_p_pair<ELEM>(ls[0], ls[1], pk[w2]);
+              fadd2(ls[0], ls[1], p0, p1);
           }
           tmem_st32(tS + half * 32, pk);
           if (half == 1) break;

@@ -390,26 +390,6 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 
 // fp32 values of the two halves of a packed bf16x2 word (exact).
 __device__ __forceinline__ float bf16lo_f32(uint32_t w) { return __uint_as_float(w << 16); }
-
-// acc0 += low half of w, acc1 += high half, each half a 16-bit float widened exactly to fp32
-// inside the add (mixed-precision add.f32.{bf16,f16}, sm_100 and later): one instruction per
-// value instead of an unpack followed by an fp32 add.
-__device__ __forceinline__ void add_bf16x2_to_f32(float& acc0, float& acc1, uint32_t w) {
-  asm("{\n\t.reg .b16 lo, hi;\n\t"
-      "mov.b32 {lo, hi}, %2;\n\t"
-      "add.rn.f32.bf16 %0, lo, %0;\n\t"
-      "add.rn.f32.bf16 %1, hi, %1;\n\t}"
-      : "+f"(acc0), "+f"(acc1)
-      : "r"(w));
-}
-__device__ __forceinline__ void add_f16x2_to_f32(float& acc0, float& acc1, uint32_t w) {
-  asm("{\n\t.reg .b16 lo, hi;\n\t"
-      "mov.b32 {lo, hi}, %2;\n\t"
-      "add.rn.f32.f16 %0, lo, %0;\n\t"
-      "add.rn.f32.f16 %1, hi, %1;\n\t}"
-      : "+f"(acc0), "+f"(acc1)
-      : "r"(w));
-}
 __device__ __forceinline__ float bf16hi_f32(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 }  // namespace sdpa

@@ -9,15 +9,18 @@ import oracle
 # Tolerances on O (absolute, vs the fp64 oracle on the same stored inputs).
 TOL_16BIT = 1e-2
 TOL_FP8 = 3e-2
-# LSE = m + ln(l) where the kernels sum l from the probabilities already rounded to the
-# 16-bit type that feeds the P.V product (so that O is normalised by exactly the weights it
-# used).  Each rounded p has relative error <= u (unit roundoff of that type), so l, a sum of
-# positive terms, has relative error <= u and |delta LSE| <= -ln(1 - u) ~ u.  Bound: u plus
-# 1e-4 for fp32 score rounding and the approximate exp2/log2 units.
+# LSE = m + ln(l).  The decode sums l from the probabilities already rounded to the 16-bit
+# type that feeds the P.V product (so that O is normalised by exactly the weights it used).
+# Each rounded p has relative error <= u (unit roundoff of that type), so l, a sum of positive
+# terms, has relative error <= u and |delta LSE| <= -ln(1 - u) ~ u.  Bound: u plus 1e-4 for
+# fp32 score rounding and the approximate exp2/log2 units.  The prefill sums the fp32
+# probabilities, so it meets these bounds with room; TOL_LSE_FP32_SUM is its own: fp32 sums of
+# at most 16384 terms (partial sums per 128-key block) and the approximate exp2/log2 units.
 U_BF16 = 2.0 ** -8
 U_F16 = 2.0 ** -11
 TOL_LSE_BF16 = U_BF16 + 1e-4   # bf16 P (bf16 inputs)
 TOL_LSE_F16 = U_F16 + 1e-4     # f16 P (f16 and e4m3 inputs)
+TOL_LSE_FP32_SUM = 1e-4        # the prefill's fp32 row sums
 TOL_LSE = TOL_LSE_BF16
 
 
