@@ -164,8 +164,8 @@ struct DecodeParams {
   int page_size, log2_page, max_pages, n_pages;
 };
 
-constexpr int kDecodeSplit = 1024;      // keys per phase-1 CTA
-constexpr int kDecodeWarps = 4;         // each warp streams kDecodeSplit / kDecodeWarps keys
+constexpr int kDecodeSplit = 2048;      // keys per phase-1 CTA (1024 measured 7-8% slower)
+constexpr int kDecodeWarps = 4;         // consumer warps: 16 keys of every 64-key chunk each
 constexpr int kDecodeDv = 128;
 
 struct MaskConvertParams {

@@ -60,9 +60,8 @@ struct PrefillCfg {
   static constexpr int OFF_K = OFF_Q + kTilesPerCta * Q_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * K_BYTES;
   static constexpr int OFF_VRAW = OFF_V + STAGES * V_BYTES;
-  // output staging of the 16-bit kernels: one 64-column box of 16-bit rows (128 x 128 B) per
-  // softmax warpgroup (the e4m3 kernels store O row by row: measured faster there)
-  static constexpr bool TMA_EPILOGUE = ELEM != kE4M3;
+  // output staging: one 64-column box of 16-bit rows (128 x 128 B) per softmax warpgroup
+  static constexpr bool TMA_EPILOGUE = true;
   static constexpr int OST_BYTES = TMA_EPILOGUE ? kBlockQ * 128 : 0;
   static constexpr int OFF_OST = OFF_VRAW + STAGES * VRAW_BYTES;
   static constexpr int OFF_BAR = OFF_OST + kTilesPerCta * OST_BYTES;
@@ -71,6 +70,7 @@ struct PrefillCfg {
   static constexpr int SMEM = OFF_BAR + 512 + 1024;
   static_assert(D % CH == 0 && DV % 64 == 0, "head dims must be multiples of 64");
   static_assert(Q_BYTES % 1024 == 0 && K_BYTES % 1024 == 0 && V_BYTES % 1024 == 0, "1 KB tile alignment");
+  static_assert(SMEM <= 227 * 1024, "more shared memory than a CTA may opt in to");
 };
 
 template <int ELEM>

@@ -319,7 +319,7 @@ int sdpa_decode_paged(const void* q, const void* k_pool, const void* v_pool, con
  * Arguments and results are those of sdpa_decode without the workspace: the per-split
  * partials go to a fixed 32 MiB array in the library's own device memory, which every GPU
  * that loads the library holds until the process exits.  A call that would need more
- * (B * Hq * ceil(max_kv / 1024) * (Dv + 2) * 4 bytes > 32 MiB) returns SDPA_ERR_UNSUPPORTED
+ * (B * Hq * ceil(max_kv / 2048) * (Dv + 2) * 4 bytes > 32 MiB) returns SDPA_ERR_UNSUPPORTED
  * and launches nothing.  The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before any stream
  * capture.  All calls on a device share the array and it keeps the last call's contents

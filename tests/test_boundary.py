@@ -37,7 +37,7 @@ def test_workspace_sizes(lib):
     assert n >= rows * nkb * 17 and n % 16 == 0
     assert fa.sdpa_fwd_workspace_size(0, 28, 1000, 3001, 128, False, True) == 0
     d = fa.sdpa_decode_workspace_size(64, 32, 16384, 128)
-    assert d == 64 * 32 * 16 * 130 * 4
+    assert d == 64 * 32 * (16384 // 2048) * 130 * 4  # [B, Hq, splits of 2048 keys, Dv + 2] fp32
     assert fa.sdpa_decode_workspace_size(0, 32, 16384, 128) == 0
 
 

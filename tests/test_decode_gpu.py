@@ -26,7 +26,8 @@ def _run(x, dtype_scale, **kw):
 @pytest.mark.parametrize("Hq,Hkv", [(32, 8), (8, 8), (16, 2), (8, 1), (12, 1), (16, 1), (32, 2)])
 @pytest.mark.parametrize("D", [128, 192])
 def test_ragged_lengths_nan_padding(dtype, Hq, Hkv, D):
-    # lengths around the 16-key step, the 256-key warp share and the 1024-key split, and 0;
+    # lengths around the 16-key step, the 64-key chunk, the 2048-key split (and the former
+    # 1024-key one), and 0;
     # padding rows are NaN, so reading any of them would poison the output.  Groups of 9-16
     # query heads use the second half of the tensor-core tile's rows; D = 192 with Dv = 128 is
     # the MLA-shaped head of the "MlaMmaOp" page.

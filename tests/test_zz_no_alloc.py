@@ -99,7 +99,7 @@ def test_noalloc_rejects_more_than_its_scratch():
     kv = torch.zeros((1, 8, 8, 128), dtype=torch.bfloat16, device=DEV)  # never read: rejected first
     kvl = torch.zeros((64,), dtype=torch.int32, device=DEV)
     o = torch.zeros((64, 32, 128), dtype=torch.bfloat16, device=DEV)
-    # 64 * 32 * ceil(65536 / 1024) * 130 * 4 bytes = 68 MB > 32 MiB
-    rc = fn(_ptr(q), _ptr(kv), _ptr(kv), _ptr(kvl), _ptr(o), None, 64, 32, 8, 65536, 128, 128, None, 0.088,
+    # 64 * 32 * ceil(131072 / 2048) * 130 * 4 bytes = 68 MB > 32 MiB
+    rc = fn(_ptr(q), _ptr(kv), _ptr(kv), _ptr(kvl), _ptr(o), None, 64, 32, 8, 131072, 128, 128, None, 0.088,
             fa.SDPA_BF16, None)
     assert rc == fa.SDPA_ERR_UNSUPPORTED
