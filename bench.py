@@ -557,6 +557,7 @@ def main_reference(args, rank, world):
     value = flops * len(ts) / total / 1e12
     cfg = config_of(w)
     cfg["l2"] = "n/a (host CPU)"
+    cfg["parallelism"] = f"replicas x{world}"  # the same key as the GPU arm's line
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total / len(ts) * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg, "impl": "reference",
